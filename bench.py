@@ -1,0 +1,345 @@
+"""Benchmark of the ZeRO-1 optimizer step: params/s and achieved HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = the whole hot path over one batch: reduce-scatter of W emulated
+ranks' bf16 gradients + global norm + clip + AdamW on the fp32 shards + bf16
+all-gather into W replicas, through the C ABI (zero1_step).  Inputs are
+seeded synthetic tensors already resident in HBM (two gradient sets used
+alternately); the working set is far larger than L2, so no flush is needed.
+
+Multi-GPU (torchrun, one process per GPU): every GPU runs its own emulated
+W-rank problem ("replicas only"); no data crosses GPUs, the process group
+serves only the barrier and the max-over-ranks time.  value = params of all
+GPUs / max time.
+
+--impl reference times the CPU oracle (single-threaded C) on the host cores,
+each step a bounded sample of the same workload; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as dt
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as WL  # noqa: E402
+
+METRIC = "ZeRO-1 step params/s and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "zero_sharded_adamw_gb300", "csrc", "zero1_kernels.cu")
+
+
+# ------------------------------------------------------------- helpers
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(world_size: int, backend: str):
+    if world_size > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world_size: int):
+    if world_size > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world_size: int, device="cpu") -> float:
+    """Max of a per-rank scalar over all ranks (identity on one rank)."""
+    if world_size == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch of the update kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"zero1_adamw_ag_kernel_{workload.replace('@', '_n')}.txt")
+    if not os.path.exists(path):
+        return None
+    with open(KERNEL_SRC, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms, kept with timestamps."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        smi = shutil.which("nvidia-smi")
+        if smi is None:
+            return
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            gpu = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            gpu = str(device_index)
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        self.out = open(self.path, "w")
+        self.proc = subprocess.Popen([smi, "-i", gpu, f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                     stdout=self.out, stderr=subprocess.DEVNULL)
+
+    def stop(self, t0: float, t1: float) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        used = inside or rows
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in used for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(used), "in_timed_region": bool(inside)}
+
+
+# -------------------------------------------------------- oracle timing
+
+def oracle_rate(w: WL.Workload, n_sample: int, steps: int, seconds: float | None = None) -> tuple[float, int, int]:
+    """Time the CPU oracle on the first n_sample parameters of workload w.
+    Runs `steps` steps (or until `seconds` have passed, if given).  Returns
+    (params/s, steps run, n_sample)."""
+    import numpy as np
+    from oracle import zero1_oracle as o
+    ws = w.with_n(n_sample)
+    hp = o.HP(**w.hparams())
+    sets = []
+    for t in (1, 2):
+        g = WL.grads(ws, t, "cpu")
+        sets.append([x.view(torch.int16).numpy().view(np.uint16) for x in g])
+    st = o.State(WL.master(ws, "cpu").numpy())
+    done, t_start = 0, time.perf_counter()
+    while True:
+        o.step(st, sets[done % 2], hp)
+        done += 1
+        el = time.perf_counter() - t_start
+        if (seconds is None and done >= steps) or (seconds is not None and el >= seconds and done >= 1):
+            break
+    return n_sample * done / el, done, n_sample
+
+
+def reference_arm(args, w: WL.Workload, cfg: dict):
+    rank, world_size, _ = dist_env()
+    if rank != 0:
+        return
+    # Size each step's sample so that warmup + timed steps end in ~60 s.
+    rate, _, _ = oracle_rate(w, 1 << 18, 1)
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    n_sample = int(min(w.n, max(4096, rate * per_step)))
+    oracle_rate(w, n_sample, max(1, args.warmup))
+    value, done, n_sample = oracle_rate(w, n_sample, args.steps)
+    sample = (f"first {n_sample:,} parameters of the {w.name} recipe, W={w.world}, "
+              f"{done} steps, single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * n_sample / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- our arm
+
+def ours_arm(args, w: WL.Workload, cfg: dict):
+    import zero_sharded_adamw_gb300 as z
+
+    rank, world_size, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    init_dist(world_size, "nccl")
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+
+    hp = z.Hparams(**w.hparams())
+    grad_sets = [WL.grads(w, t, dev) for t in (1, 2)]
+    reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
+    opt = z.Zero1(w.n, w.world, hp)
+    opt.set_state(WL.master(w, dev), stream=stream)
+    torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        opt.step(grad_sets[i % 2], reps, stream)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3 if clocks.proc else 0.0)
+    z.zero1_profile_start(opt.handle, args.steps)
+    barrier(world_size)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        opt.step(grad_sets[i % 2], reps, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world_size)
+    t1 = time.time()
+    local_ms = ev0.elapsed_time(ev1)
+    rs_ms, upd_ms, prof_steps = z.zero1_profile_stop(opt.handle)
+    clk = clocks.stop(t0, t1)
+    ms = reduce_max(local_ms, world_size, dev)
+    norm, clip = opt.grad_norm(stream)
+
+    ms_per_step = ms / args.steps
+    value = world_size * w.n * args.steps / (ms / 1e3)
+    alg_step = w.bytes_per_step()
+    peak, peak_kind = measured_peak()
+    upd_avg = upd_ms / max(1, prof_steps)
+    rs_avg = rs_ms / max(1, prof_steps)
+    upd_bytes = (24 + 2 * w.world) * w.n          # state read+write, replica writes
+    rs_bytes = (2 * w.world) * w.n                # gradient reads
+    traffic = kernel_traffic(w.name)
+    achieved = upd_bytes / (upd_avg / 1e3) / 1e9
+
+    # End to end through the host-buffer entry point: H2D of every rank's
+    # gradient from pinned memory, the step, D2H of every rank's replica.
+    e2e = None
+    if not args.no_e2e:
+        hg = [g.cpu().pin_memory() for g in grad_sets[0]]
+        hr = [torch.empty(w.n, dtype=torch.bfloat16).pin_memory() for _ in range(w.world)]
+        k_e2e = max(3, min(args.steps, 20))
+        opt.step_host(hg, hr, stream)              # allocates the staging buffers
+        barrier(world_size)
+        torch.cuda.synchronize(dev)
+        s0 = time.perf_counter()
+        for _ in range(k_e2e):
+            opt.step_host(hg, hr, stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = reduce_max(time.perf_counter() - s0, world_size, dev)
+        e2e = {"value": world_size * w.n * k_e2e / e2e_s, "unit": "params/s",
+               "h2d_bytes_per_step": 2 * w.world * w.n, "d2h_bytes_per_step": 2 * w.world * w.n,
+               "steps": k_e2e, "entry_point": "zero1_step_host"}
+        del hg, hr
+
+    cpu = None
+    if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
+        rate, done, n_s = oracle_rate(w, 1 << 20, 1, seconds=10.0)
+        cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n_s:,} parameters of the {w.name} recipe, W={w.world}, {done} steps "
+                         f"(~10 s), single-threaded C oracle"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world_size,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+        "hbm": {"algorithmic_bytes_per_step": alg_step,
+                "algorithmic_gbs": world_size * alg_step / (ms_per_step / 1e3) / 1e9,
+                "frac_of_peak": (alg_step / (ms_per_step / 1e3) / 1e9) / peak,
+                "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": "zero1_adamw_ag_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": upd_bytes, "avg_launch_ms": upd_avg,
+                     "peak_kind": peak_kind},
+        "kernels": {
+            "zero1_rs_norm_kernel": {"avg_launch_ms": rs_avg, "algorithmic_bytes": rs_bytes,
+                                     "gbs": rs_bytes / (rs_avg / 1e3) / 1e9},
+            "zero1_adamw_ag_kernel": {"avg_launch_ms": upd_avg, "algorithmic_bytes": upd_bytes,
+                                      "gbs": achieved},
+            "launches_timed": prof_steps},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": 2 * args.steps,
+        "last_step": {"grad_norm": norm, "clip_coef": clip},
+    }
+    opt.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world_size > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gpt2_small", choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the workload's parameter count (same recipe; small profiling cases)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WL.WORKLOADS[args.workload]
+    if args.n is not None:
+        w = w.with_n(args.n)
+    cfg = {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
+           "bytes_per_param": 4 * w.world + 24, "hparams": w.hparams(),
+           "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
+           "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
+                 else "working set fits in L2 (launch-latency bound)"}
+    if args.impl == "reference":
+        reference_arm(args, w, cfg)
+    else:
+        ours_arm(args, w, cfg)
+
+
+if __name__ == "__main__":
+    main()

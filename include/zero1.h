@@ -1,0 +1,196 @@
+/*
+ * zero1.h -- C ABI of a GB300 (sm_103a) ZeRO-1 data-parallel optimizer step.
+ *
+ * One step of ZeRO stage 1 over W data-parallel ranks:
+ *   1. reduce-scatter of the W ranks' bf16 gradients: rank r receives slice r
+ *      of the rank-ordered fp32 sum, scaled by 1/W (gradient averaging);
+ *   2. the global L2 norm of the averaged gradient and the clip coefficient;
+ *   3. AdamW on each rank's fp32 master / m / v slice;
+ *   4. bf16 cast of the updated master and all-gather into all W replicas.
+ *
+ * Sources (web pages, cited by title and section):
+ *   "Stanford CS336 Lecture 7 close reading: Parallelism (part 1)",
+ *     section 5.2 (ZeRO stage 1: reduce-scatter, per-slice update with the
+ *     slice's own optimizer state, all-gather of the updated parameters).
+ *   "Stanford CS336 Lecture 8 close reading: Parallelism (part 2)",
+ *     section 2 (all-reduce = reduce-scatter + all-gather) and section 7
+ *     (data parallel: gradients averaged with ReduceOp.AVG).
+ *   "Parallel training" (notes.cassieliang.com), section "What one card
+ *     holds: mixed precision and AdamW" (fp32 master, m, v; the update with
+ *     folded bias correction and decoupled decay after the update; bf16 copy
+ *     for the forward), section "Training loop and checkpoint" (global-norm
+ *     clipping; a checkpoint holds m, v and the step count t).
+ *
+ * Emulation: the W ranks live in one GPU's memory.  Rank r's gradient and
+ * parameter replica are caller buffers grad_ptrs[r] and param_ptrs[r]; the
+ * library owns the fp32 optimizer state of all W slices.  No collective
+ * library is involved: the reduce-scatter is a rank-ordered read of the W
+ * gradient buffers and the all-gather is a W-way store.
+ *
+ * Conventions for every entry point:
+ *   - Return 0 on success or a negative ZERO1_E* code; zero1_last_error()
+ *     then holds a message (thread-local).  Nothing aborts the process.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued on it; calls return without waiting
+ *     unless stated.
+ *   - Device buffers must be 16-byte aligned (ZERO1_EALIGN otherwise).
+ *   - A handle is used by one host thread and one stream at a time.
+ *   - Numerics: no FMA contraction on the reduce-scatter sums and the AdamW
+ *     update; every fp32 operation is IEEE round-to-nearest-even, so for a
+ *     given clip coefficient the state and replicas are bit-for-bit those of
+ *     the plain fp32 definition.  The norm is accumulated in compensated fp32
+ *     per thread and fp64 across threads, in a fixed order (deterministic for
+ *     a given n, W and device).
+ */
+#ifndef ZERO1_H
+#define ZERO1_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO1_OK        0
+#define ZERO1_EINVAL   -1   /* null pointer, n = 0, bad world size, bad hyperparameter, bad handle */
+#define ZERO1_EALIGN   -2   /* a device buffer is not 16-byte aligned                             */
+#define ZERO1_ENOMEM   -3   /* a device allocation failed                                         */
+#define ZERO1_ECUDA    -4   /* a CUDA runtime call or a kernel launch failed                      */
+#define ZERO1_ENODEV   -5   /* no CUDA device, or the device is not compute capability 10.3      */
+
+/* Largest number of emulated ranks one handle accepts. */
+#define ZERO1_MAX_WORLD 512
+
+/* AdamW + clipping hyperparameters.
+ *   lr, beta1, beta2, eps, weight_decay: the AdamW update
+ *       m = beta1*m + (1-beta1)*g,  v = beta2*v + (1-beta2)*g*g,
+ *       p = p - lr*sqrt(1-beta2^t)/(1-beta1^t) * m/(sqrt(v)+eps),
+ *       p = p * (1 - lr*weight_decay)
+ *     ("Parallel training", "mixed precision and AdamW").  0 <= beta < 1,
+ *     eps >= 0, lr >= 0, weight_decay >= 0.
+ *   max_norm: global-norm clipping threshold; <= 0 disables clipping
+ *     ("Parallel training", "training loop and checkpoint"). */
+typedef struct zero1_hparams {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+    double max_norm;
+} zero1_hparams;
+
+typedef struct zero1_ctx *zero1_handle;
+
+/* Create an optimizer for n parameters over `world` emulated ranks.
+ * Allocates the fp32 master, m and v (each W*S floats, S the shard length
+ * below) plus scratch on the current CUDA device with cudaMalloc; m = v = 0,
+ * master = 0, t = 0.  Load real weights with zero1_set_state.
+ * Shards: rank r owns parameters [r*S, min((r+1)*S, n)) with
+ * S = ceil(n/W) rounded up to a multiple of 64 (256-byte aligned shard
+ * starts); the padding past n is never read or written by a step.
+ * Scratch: W >= 3 keeps the fp32 reduce-scatter result (4*W*S bytes) between
+ * the two kernels; W <= 2 re-reads the gradients instead (cheaper in bytes).
+ * Errors: ZERO1_EINVAL (out == NULL, hp == NULL, n == 0, world outside
+ * [1, ZERO1_MAX_WORLD], bad hyperparameters), ZERO1_ENODEV, ZERO1_ENOMEM.
+ * On error *out is set to NULL. */
+int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *out);
+
+/* Free the handle and its device memory after synchronizing the device.
+ * NULL is accepted and ignored.  Returns ZERO1_OK or ZERO1_ECUDA. */
+int zero1_destroy(zero1_handle h);
+
+/* One ZeRO-1 step (t -> t+1) on `stream`, fully asynchronous, allocation-free.
+ *   grad_ptrs:  host array of W device pointers; rank r's bf16 gradient,
+ *               n entries, 16-byte aligned.  Only read.
+ *   param_ptrs: host array of W device pointers; rank r's bf16 parameter
+ *               replica, n entries, 16-byte aligned.  Only written: every
+ *               replica receives bf16(master) of all n parameters.
+ * The pointer arrays themselves are copied into the launch; the buffers must
+ * stay valid until the stream reaches the step.  Gradient and replica
+ * buffers must not overlap each other or the library's state.
+ * Launches exactly two kernels: the reduce-scatter + norm kernel and the
+ * clip + AdamW + bf16 + all-gather kernel.
+ * Errors: ZERO1_EINVAL (NULL handle / array / entry), ZERO1_EALIGN,
+ * ZERO1_ECUDA (launch failure; t is then left unchanged). */
+int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_ptrs, void *stream);
+
+/* The same step for callers whose gradients and replicas live in host
+ * memory: copies the W host gradients to device staging buffers, runs
+ * zero1_step, copies the W replicas back, and waits for the stream.
+ *   host_grads:  W host pointers, n bf16 each (pinned memory recommended).
+ *   host_params: W host pointers, n bf16 each, written.
+ * The first call allocates the staging buffers (4*W*n bytes, freed by
+ * zero1_destroy).  Errors as zero1_step, plus ZERO1_ENOMEM. */
+int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
+
+/* Checkpoint restore ("Parallel training", "training loop and checkpoint":
+ * a checkpoint carries m, v and t).  master, m, v: fp32 arrays of n entries
+ * in device or host memory (copied with cudaMemcpyDefault); m or v may be
+ * NULL, meaning zeros.  t: the number of steps already taken (the next step
+ * uses t+1).  Enqueued on `stream`; a pageable host source is consumed
+ * before the call returns.  Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
+int zero1_set_state(zero1_handle h, const float *master, const float *m, const float *v,
+                    uint64_t t, void *stream);
+
+/* Checkpoint save: copies master, m, v (n fp32 each) into device or host
+ * arrays (any may be NULL to skip it) and writes the step count to *t (may
+ * be NULL).  Enqueued on `stream`; synchronize it before reading a host
+ * destination. */
+int zero1_get_state(zero1_handle h, float *master, float *m, float *v, uint64_t *t, void *stream);
+
+/* The same two copies for parameters [offset, offset+count) only -- one
+ * rank's shard is offset = r*S, count = min(S, n - r*S) -- so that each rank
+ * can save or load its own slice.  The step count is untouched.
+ * Errors: ZERO1_EINVAL (range outside [0, n), NULL master for set). */
+int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const float *master,
+                          const float *m, const float *v, void *stream);
+int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float *master,
+                          float *m, float *v, void *stream);
+
+/* Change the learning rate used by later steps (schedules such as warmup +
+ * cosine, "Parallel training", "training loop and checkpoint").
+ * Errors: ZERO1_EINVAL for a NULL handle or lr < 0 or not finite. */
+int zero1_set_lr(zero1_handle h, double lr);
+
+/* Norm of the averaged gradient of the latest step and the clip coefficient
+ * it applied (1 when not clipped).  Waits for `stream`.  Either output may
+ * be NULL.  Before the first step both read 0. */
+int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *stream);
+
+/* Layout facts: the shard length S, the padded state length W*S, and the
+ * bytes of device memory the handle holds (state + scratch, excluding the
+ * host-path staging buffers).  Any output may be NULL. */
+int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint64_t *device_bytes);
+
+/* Per-kernel timing.  After zero1_profile_start, each of the next
+ * `capacity` steps records three CUDA events on its stream (before the
+ * reduce-scatter + norm kernel, between the kernels, after the update +
+ * all-gather kernel).  zero1_profile_stop waits for the last recorded event
+ * and returns the summed kernel times in milliseconds and the number of
+ * steps recorded; it frees the events.  Either kernel's average launch
+ * duration is its sum divided by *steps.  Outputs may be NULL.
+ * Errors: ZERO1_EINVAL (capacity < 1, or stop without start), ZERO1_ECUDA. */
+int zero1_profile_start(zero1_handle h, int capacity);
+int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, uint64_t *steps);
+
+/* Host-only planning (no device needed).  The shard length S = ceil(n/W)
+ * rounded up to 64 and the padded state length W*S for n parameters over
+ * `world` ranks.  Errors: ZERO1_EINVAL (n == 0 or world out of range). */
+int zero1_shard_plan(uint64_t n, int world, uint64_t *shard_len, uint64_t *padded_len);
+
+/* Host-only: the fp32 scalars step number t (1-based) multiplies with,
+ * formed in double and rounded once ("Parallel training", "mixed precision
+ * and AdamW"): out[0..7] = 1/W, beta1, 1-beta1, beta2, 1-beta2,
+ * lr*sqrt(1-beta2^t)/(1-beta1^t), 1-lr*weight_decay, eps.
+ * Errors: ZERO1_EINVAL (NULL pointer, t == 0, bad world or hyperparameter). */
+int zero1_step_scalars(const zero1_hparams *hp, int world, uint64_t t, float out[8]);
+
+/* Message for the last error on this thread ("" if none). */
+const char *zero1_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO1_H */

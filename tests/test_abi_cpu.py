@@ -1,0 +1,99 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry
+point include/zero1.h declares, and its host logic (shard plan, per-step
+scalars, argument checks) agrees with the oracle.  No compute call runs."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import zero_sharded_adamw_gb300 as z
+from oracle import zero1_oracle as o
+from zero_sharded_adamw_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zero1.h")
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    return _build.build()
+
+
+def declared_symbols() -> set[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(zero1_\w+)\s*\(", text, flags=re.M))
+
+
+def test_exports_every_declared_symbol(lib_path):
+    declared = declared_symbols()
+    assert "zero1_create" in declared and "zero1_step" in declared and "zero1_destroy" in declared
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (zero1_\w+)$", out, flags=re.M))
+    assert declared <= exported, declared - exported
+    assert declared == set(z.EXPORTED_SYMBOLS)
+    lib = C.CDLL(lib_path)
+    for name in declared:
+        assert getattr(lib, name)
+
+
+def test_shard_plan_matches_oracle_chunks(lib_path):
+    for n in (1, 7, 8, 9, 13, 4095, 4096, 4097, 124_355_328, 1_300_000_005, 7_000_000_000, 350_000_000):
+        for world in (1, 2, 3, 4, 8, 64, 512):
+            s, padded = z.zero1_shard_plan(n, world)
+            so = o.shard_len(n, world)
+            assert s % 64 == 0 and so <= s < so + 64 and padded == s * world
+            assert padded - n < world * 64                      # padding below 64 per shard
+            covered = sum(max(0, min((r + 1) * s, n) - min(r * s, n)) for r in range(world))
+            assert covered == n
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 64])
+@pytest.mark.parametrize("t", [1, 2, 10, 1000])
+def test_step_scalars_match_oracle(lib_path, world, t):
+    for hp in (dict(), dict(lr=3e-4, beta1=0.8, beta2=0.999, eps=1e-6, weight_decay=0.01),
+               dict(lr=1e-3, beta1=0.0, beta2=0.0, eps=0.0, weight_decay=0.0, max_norm=0.0)):
+        ours = z.zero1_step_scalars(z.Hparams(**hp), world, t)
+        ref = o.step_scalars(o.HP(**hp), world, t)
+        for k in ref:
+            assert np.float32(ours[k]).view(np.uint32) == np.float32(ref[k]).view(np.uint32), (k, hp)
+
+
+def test_argument_checks_before_any_device_call(lib_path):
+    bad = [(0, 4, {}), (10, 0, {}), (10, z.ZERO1_MAX_WORLD + 1, {}), (10, 4, {"beta1": 1.0}),
+           (10, 4, {"beta2": -0.1}), (10, 4, {"lr": float("nan")}), (10, 4, {"eps": -1.0}),
+           (10, 4, {"weight_decay": float("inf")}), (10, 4, {"max_norm": float("nan")})]
+    for n, world, hp in bad:
+        with pytest.raises(z.Zero1Error) as e:
+            z.zero1_create(n, world, z.Hparams(**hp))
+        assert e.value.code == -1, (n, world, hp, str(e.value))
+    with pytest.raises(z.Zero1Error) as e:
+        z.zero1_step_scalars(z.Hparams(), 4, 0)
+    assert e.value.code == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_create_without_device_reports_enodev(lib_path):
+    with pytest.raises(z.Zero1Error) as e:
+        z.zero1_create(4096, 4)
+    assert e.value.code == -5
+
+
+def test_unknown_handles_are_rejected_not_dereferenced(lib_path):
+    bogus = 0xDEAD0000
+    for call in (lambda: z.zero1_step(bogus, [16] * 4, [16] * 4),
+                 lambda: z.zero1_set_lr(bogus, 1e-3),
+                 lambda: z.zero1_layout(bogus),
+                 lambda: z.zero1_get_state(bogus),
+                 lambda: z.zero1_destroy(bogus),
+                 lambda: z.zero1_step(None, [16], [16])):
+        with pytest.raises(z.Zero1Error) as e:
+            call()
+        assert e.value.code == -1
+    z.zero1_destroy(None)                      # NULL is accepted
+    assert "invalid handle" in z.zero1_last_error() or z.zero1_last_error() == ""

@@ -1,0 +1,265 @@
+"""GB300 (sm_103a) ZeRO-1 data-parallel optimizer step.
+
+A thin ctypes binding of ``libzero1.so`` (C ABI in ``include/zero1.h``): the
+functions below carry the C entry points' names and only marshal arguments.
+Every step of the path runs in the library's two CUDA kernels; there is no
+CPU fallback.  The library is built by ``__graft_entry__.build()`` (or
+``python -m zero_sharded_adamw_gb300._build``); calling any entry point
+without it raises ``Zero1Error``.
+
+Pointers may be given as ints or as objects with ``data_ptr()`` (torch
+tensors) or ``ctypes.data`` (numpy arrays).  Streams may be ints, objects
+with ``cuda_stream`` (torch streams) or None (the legacy default stream).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+__all__ = [
+    "Zero1Error", "Hparams", "Zero1",
+    "zero1_create", "zero1_destroy", "zero1_step", "zero1_step_host",
+    "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
+    "zero1_set_lr", "zero1_get_grad_norm",
+    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_last_error",
+    "library_path", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libzero1.so")
+
+ZERO1_MAX_WORLD = 512
+ERRORS = {-1: "ZERO1_EINVAL", -2: "ZERO1_EALIGN", -3: "ZERO1_ENOMEM", -4: "ZERO1_ECUDA", -5: "ZERO1_ENODEV"}
+
+# Every entry point include/zero1.h declares, with its ctypes signature.
+_P, _U64, _I32, _F64 = C.c_void_p, C.c_uint64, C.c_int, C.c_double
+_SIGS = {
+    "zero1_create": (_I32, [_U64, _I32, _P, _P]),
+    "zero1_destroy": (_I32, [_P]),
+    "zero1_step": (_I32, [_P, _P, _P, _P]),
+    "zero1_step_host": (_I32, [_P, _P, _P, _P]),
+    "zero1_set_state": (_I32, [_P, _P, _P, _P, _U64, _P]),
+    "zero1_get_state": (_I32, [_P, _P, _P, _P, _P, _P]),
+    "zero1_set_state_range": (_I32, [_P, _U64, _U64, _P, _P, _P, _P]),
+    "zero1_get_state_range": (_I32, [_P, _U64, _U64, _P, _P, _P, _P]),
+    "zero1_set_lr": (_I32, [_P, _F64]),
+    "zero1_get_grad_norm": (_I32, [_P, _P, _P, _P]),
+    "zero1_layout": (_I32, [_P, _P, _P, _P]),
+    "zero1_profile_start": (_I32, [_P, _I32]),
+    "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
+    "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
+    "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
+    "zero1_last_error": (C.c_char_p, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+
+class Zero1Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {message}")
+        self.code = code
+
+
+class _CHparams(C.Structure):
+    _fields_ = [(k, C.c_double) for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_norm")]
+
+
+@dataclass
+class Hparams:
+    """AdamW + clipping hyperparameters; max_norm <= 0 disables clipping."""
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+    max_norm: float = 1.0
+
+    def _c(self) -> _CHparams:
+        return _CHparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.max_norm)
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise Zero1Error(-5, f"{_LIB_PATH} is not built; run "
+                                 "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise Zero1Error(rc, _load().zero1_last_error().decode())
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    return int(s.cuda_stream) or None
+
+
+def _ptrs(xs) -> C.Array:
+    return (C.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+
+# --------------------------------------------------------- entry points
+
+def zero1_last_error() -> str:
+    return _load().zero1_last_error().decode()
+
+
+def zero1_create(n: int, world: int, hp: Hparams | None = None) -> int:
+    """Create a handle for n parameters over `world` emulated ranks."""
+    h = C.c_void_p()
+    c = (hp or Hparams())._c()
+    _check(_load().zero1_create(n, world, C.byref(c), C.byref(h)))
+    return h.value
+
+
+def zero1_destroy(h: int | None) -> None:
+    _check(_load().zero1_destroy(h))
+
+
+def zero1_step(h: int, grad_ptrs, param_ptrs, stream=None) -> None:
+    """One step: W device gradient buffers in, W device replicas out."""
+    _check(_load().zero1_step(h, _ptrs(grad_ptrs), _ptrs(param_ptrs), _stream(stream)))
+
+
+def zero1_step_host(h: int, host_grads, host_params, stream=None) -> None:
+    """One step from host gradient buffers into host replica buffers (waits)."""
+    _check(_load().zero1_step_host(h, _ptrs(host_grads), _ptrs(host_params), _stream(stream)))
+
+
+def zero1_set_state(h: int, master, m=None, v=None, t: int = 0, stream=None) -> None:
+    _check(_load().zero1_set_state(h, _addr(master), _addr(m), _addr(v), t, _stream(stream)))
+
+
+def zero1_get_state(h: int, master=None, m=None, v=None, stream=None) -> int:
+    t = C.c_uint64()
+    _check(_load().zero1_get_state(h, _addr(master), _addr(m), _addr(v), C.byref(t), _stream(stream)))
+    return t.value
+
+
+def zero1_set_state_range(h: int, offset: int, count: int, master, m=None, v=None, stream=None) -> None:
+    _check(_load().zero1_set_state_range(h, offset, count, _addr(master), _addr(m), _addr(v), _stream(stream)))
+
+
+def zero1_get_state_range(h: int, offset: int, count: int, master=None, m=None, v=None, stream=None) -> None:
+    _check(_load().zero1_get_state_range(h, offset, count, _addr(master), _addr(m), _addr(v), _stream(stream)))
+
+
+def zero1_set_lr(h: int, lr: float) -> None:
+    _check(_load().zero1_set_lr(h, lr))
+
+
+def zero1_get_grad_norm(h: int, stream=None) -> tuple[float, float]:
+    norm, clip = C.c_double(), C.c_float()
+    _check(_load().zero1_get_grad_norm(h, C.byref(norm), C.byref(clip), _stream(stream)))
+    return norm.value, clip.value
+
+
+def zero1_layout(h: int) -> tuple[int, int, int]:
+    s, p, b = C.c_uint64(), C.c_uint64(), C.c_uint64()
+    _check(_load().zero1_layout(h, C.byref(s), C.byref(p), C.byref(b)))
+    return s.value, p.value, b.value
+
+
+def zero1_profile_start(h: int, capacity: int) -> None:
+    _check(_load().zero1_profile_start(h, capacity))
+
+
+def zero1_profile_stop(h: int) -> tuple[float, float, int]:
+    """(summed reduce-scatter+norm ms, summed update+all-gather ms, steps)."""
+    a, b, n = C.c_double(), C.c_double(), C.c_uint64()
+    _check(_load().zero1_profile_stop(h, C.byref(a), C.byref(b), C.byref(n)))
+    return a.value, b.value, n.value
+
+
+def zero1_shard_plan(n: int, world: int) -> tuple[int, int]:
+    """Shard length S and padded length W*S (host only, no device)."""
+    s, p = C.c_uint64(), C.c_uint64()
+    _check(_load().zero1_shard_plan(n, world, C.byref(s), C.byref(p)))
+    return s.value, p.value
+
+
+def zero1_step_scalars(hp: Hparams, world: int, t: int) -> dict:
+    """The fp32 scalars step t uses (host only, no device)."""
+    out = (C.c_float * 8)()
+    c = hp._c()
+    _check(_load().zero1_step_scalars(C.byref(c), world, t, out))
+    keys = ("inv_w", "beta1", "one_minus_beta1", "beta2", "one_minus_beta2", "step_size", "decay", "eps")
+    return dict(zip(keys, list(out)))
+
+
+class Zero1:
+    """Owning wrapper around a handle (closes on ``close()`` / context exit)."""
+
+    def __init__(self, n: int, world: int, hp: Hparams | None = None):
+        self.n, self.world, self.hp = n, world, hp or Hparams()
+        self.handle = zero1_create(n, world, self.hp)
+
+    def step(self, grads, params, stream=None) -> None:
+        zero1_step(self.handle, grads, params, stream)
+
+    def step_host(self, grads, params, stream=None) -> None:
+        zero1_step_host(self.handle, grads, params, stream)
+
+    def set_state(self, master, m=None, v=None, t: int = 0, stream=None) -> None:
+        zero1_set_state(self.handle, master, m, v, t, stream)
+
+    def get_state(self, master=None, m=None, v=None, stream=None) -> int:
+        return zero1_get_state(self.handle, master, m, v, stream)
+
+    def set_lr(self, lr: float) -> None:
+        zero1_set_lr(self.handle, lr)
+
+    def grad_norm(self, stream=None) -> tuple[float, float]:
+        return zero1_get_grad_norm(self.handle, stream)
+
+    def layout(self) -> tuple[int, int, int]:
+        return zero1_layout(self.handle)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            zero1_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,447 @@
+// zero1_host.cu -- the C ABI declared in include/zero1.h: argument checks,
+// the shard plan, per-step scalars, device memory, and the launches.
+//
+// Shard plan ("Stanford CS336 Lecture 7 close reading: Parallelism (part 1)",
+// 5.2; equal chunks as "Stanford CS336 Lecture 8 close reading: Parallelism
+// (part 2)", section 2, requires of a reduce-scatter): S = ceil(n/W) rounded
+// up to 64, rank r owns [r*S, min((r+1)*S, n)).  In one GPU's memory the W
+// fp32 shards of master, m and v sit end to end, so parameter i's state is
+// at index i of each array and a launch covers all ranks' shards at once.
+//
+// Per-step scalars ("Parallel training", "mixed precision and AdamW"):
+// formed in double, rounded once to fp32 -- step_size = lr*sqrt(1-beta2^t)/
+// (1-beta1^t), decay = 1 - lr*wd, 1-beta1, 1-beta2, 1/W.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include "zero1.h"
+#include "zero1_internal.h"
+
+struct zero1_ctx {
+    uint64_t n = 0;
+    int world = 0;
+    zero1_hparams hp{};
+    uint64_t t = 0;              // steps taken
+    uint64_t shard = 0;          // S
+    uint64_t padded = 0;         // W * S
+    int device = 0;
+    int num_sms = 0;
+    int grid_rs = 0, grid_update = 0;
+    bool reread = false;         // W <= 2: the update kernel re-reads the gradients
+    void *block = nullptr;       // one cudaMalloc holding everything below
+    uint64_t block_bytes = 0;
+    float *master = nullptr, *m = nullptr, *v = nullptr, *ghat = nullptr;
+    double *partials = nullptr;
+    zero1::DevStatus *status = nullptr;
+    // host-path staging (zero1_step_host), allocated on first use
+    void *staging = nullptr;
+    uint64_t staging_stride = 0;
+    // per-kernel timing (zero1_profile_start/stop): 3 events per step
+    std::vector<cudaEvent_t> prof;
+    int prof_capacity = 0, prof_used = 0;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    if (e == cudaErrorMemoryAllocation)
+        return fail(ZERO1_ENOMEM, "%s: %s", what, cudaGetErrorString(e));
+    return fail(ZERO1_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::mutex g_mu;
+std::unordered_set<zero1_ctx *> g_live;
+
+bool live(zero1_ctx *h)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    return h != nullptr && g_live.count(h) != 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+bool finite_nonneg(double x) { return std::isfinite(x) && x >= 0.0; }
+
+int check_hparams(const zero1_hparams *hp)
+{
+    if (!finite_nonneg(hp->lr)) return fail(ZERO1_EINVAL, "lr must be finite and >= 0");
+    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0)) return fail(ZERO1_EINVAL, "beta1 must be in [0, 1)");
+    if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0)) return fail(ZERO1_EINVAL, "beta2 must be in [0, 1)");
+    if (!finite_nonneg(hp->eps)) return fail(ZERO1_EINVAL, "eps must be finite and >= 0");
+    if (!finite_nonneg(hp->weight_decay)) return fail(ZERO1_EINVAL, "weight_decay must be finite and >= 0");
+    if (std::isnan(hp->max_norm)) return fail(ZERO1_EINVAL, "max_norm must not be NaN");
+    return ZERO1_OK;
+}
+
+zero1::StepScalars step_scalars(const zero1_hparams &hp, int world, uint64_t t)
+{
+    const double bc1 = 1.0 - std::pow(hp.beta1, (double)t);
+    const double bc2 = 1.0 - std::pow(hp.beta2, (double)t);
+    zero1::StepScalars s;
+    s.inv_w = (float)(1.0 / (double)world);
+    s.beta1 = (float)hp.beta1;
+    s.omb1 = (float)(1.0 - hp.beta1);
+    s.beta2 = (float)hp.beta2;
+    s.omb2 = (float)(1.0 - hp.beta2);
+    s.step_size = (float)(hp.lr * std::sqrt(bc2) / bc1);
+    s.decay = (float)(1.0 - hp.lr * hp.weight_decay);
+    s.eps = (float)hp.eps;
+    return s;
+}
+
+// Make the handle's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char *zero1_last_error(void) { return g_err; }
+
+int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *out)
+{
+    g_err[0] = '\0';
+    if (out == nullptr) return fail(ZERO1_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (hp == nullptr) return fail(ZERO1_EINVAL, "hparams is NULL");
+    if (n == 0) return fail(ZERO1_EINVAL, "n must be > 0");
+    if (world < 1 || world > ZERO1_MAX_WORLD)
+        return fail(ZERO1_EINVAL, "world must be in [1, %d], got %d", ZERO1_MAX_WORLD, world);
+    if (n > (uint64_t)1 << 50) return fail(ZERO1_EINVAL, "n too large");
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+
+    int dev = 0, count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess || count == 0)
+        return fail(ZERO1_ENODEV, "no CUDA device (%s)", cudaGetErrorString(e));
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(ZERO1_ENODEV, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major, prop.minor);
+
+    zero1_ctx *h = new (std::nothrow) zero1_ctx;
+    if (!h) return fail(ZERO1_ENOMEM, "host allocation failed");
+    h->n = n;
+    h->world = world;
+    h->hp = *hp;
+    h->device = dev;
+    h->num_sms = prop.multiProcessorCount;
+    zero1_shard_plan(n, world, &h->shard, &h->padded);
+    h->reread = world <= 2;
+    zero1::plan_grids(world, n, h->reread, h->num_sms, &h->grid_rs, &h->grid_update);
+
+    // One allocation: master | m | v | ghat (W >= 3) | partials | status,
+    // every section 256-byte aligned.
+    const uint64_t state_bytes = round_up(h->padded * sizeof(float), 256);
+    const uint64_t ghat_bytes = h->reread ? 0 : state_bytes;
+    const uint64_t part_bytes = round_up(2 * (uint64_t)h->grid_rs * sizeof(double), 256);
+    const uint64_t status_bytes = 256;
+    h->block_bytes = 3 * state_bytes + ghat_bytes + part_bytes + status_bytes;
+    if ((e = cudaMalloc(&h->block, h->block_bytes)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaMalloc of optimizer state");
+    }
+    char *base = static_cast<char *>(h->block);
+    h->master = reinterpret_cast<float *>(base);
+    h->m = reinterpret_cast<float *>(base + state_bytes);
+    h->v = reinterpret_cast<float *>(base + 2 * state_bytes);
+    h->ghat = h->reread ? nullptr : reinterpret_cast<float *>(base + 3 * state_bytes);
+    h->partials = reinterpret_cast<double *>(base + 3 * state_bytes + ghat_bytes);
+    h->status = reinterpret_cast<zero1::DevStatus *>(base + 3 * state_bytes + ghat_bytes + part_bytes);
+    if ((e = cudaMemset(h->block, 0, h->block_bytes)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cudaFree(h->block);
+        delete h;
+        return cuda_fail(e, "cudaMemset of optimizer state");
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_live.insert(h);
+    }
+    *out = h;
+    return ZERO1_OK;
+}
+
+int zero1_destroy(zero1_handle h)
+{
+    if (h == nullptr) return ZERO1_OK;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_live.erase(h)) return fail(ZERO1_EINVAL, "unknown or already destroyed handle");
+    }
+    DeviceGuard g(h->device);
+    cudaError_t e1 = cudaDeviceSynchronize();
+    cudaError_t e2 = cudaFree(h->block);
+    cudaError_t e3 = h->staging ? cudaFree(h->staging) : cudaSuccess;
+    for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
+    delete h;
+    if (e1 != cudaSuccess) return cuda_fail(e1, "cudaDeviceSynchronize in destroy");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
+    if (e3 != cudaSuccess) return cuda_fail(e3, "cudaFree staging");
+    return ZERO1_OK;
+}
+
+int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!grad_ptrs || !param_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r) {
+        if (!grad_ptrs[r] || !param_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
+        if (!aligned16(grad_ptrs[r]) || !aligned16(param_ptrs[r]))
+            return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+    }
+    DeviceGuard g(h->device);
+    zero1::StepLaunch s;
+    s.grads = grad_ptrs;
+    s.params = param_ptrs;
+    s.world = h->world;
+    s.n = h->n;
+    s.master = h->master;
+    s.m = h->m;
+    s.v = h->v;
+    s.ghat = h->ghat;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    s.grid_rs = h->grid_rs;
+    s.grid_update = h->grid_update;
+    cudaEvent_t *ev = nullptr;
+    if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
+    cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    if (ev) h->prof_used += 1;
+    h->t += 1;
+    return ZERO1_OK;
+}
+
+int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!host_grads || !host_params) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r)
+        if (!host_grads[r] || !host_params[r]) return fail(ZERO1_EINVAL, "rank %d host buffer is NULL", r);
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t bytes = h->n * 2;
+    cudaError_t e;
+    if (!h->staging) {
+        h->staging_stride = round_up(bytes, 256);
+        if ((e = cudaMalloc(&h->staging, 2 * (uint64_t)h->world * h->staging_stride)) != cudaSuccess) {
+            h->staging = nullptr;
+            return cuda_fail(e, "cudaMalloc of staging buffers");
+        }
+    }
+    const void *dg[ZERO1_MAX_WORLD];
+    void *dp[ZERO1_MAX_WORLD];
+    char *base = static_cast<char *>(h->staging);
+    for (int r = 0; r < h->world; ++r) {
+        dg[r] = base + (uint64_t)r * h->staging_stride;
+        dp[r] = base + (uint64_t)(h->world + r) * h->staging_stride;
+        if ((e = cudaMemcpyAsync(const_cast<void *>(dg[r]), host_grads[r], bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(e, "host-to-device gradient copy");
+    }
+    int rc = zero1_step(h, dg, dp, stream);
+    if (rc) return rc;
+    for (int r = 0; r < h->world; ++r)
+        if ((e = cudaMemcpyAsync(host_params[r], dp[r], bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host replica copy");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return ZERO1_OK;
+}
+
+int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const float *master,
+                          const float *m, const float *v, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!master) return fail(ZERO1_EINVAL, "master is NULL");
+    if (offset > h->n || count > h->n - offset) return fail(ZERO1_EINVAL, "range outside [0, n)");
+    if (count == 0) return ZERO1_OK;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t bytes = count * sizeof(float);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->master + offset, master, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+        return cuda_fail(e, "master copy");
+    e = m ? cudaMemcpyAsync(h->m + offset, m, bytes, cudaMemcpyDefault, st)
+          : cudaMemsetAsync(h->m + offset, 0, bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "m copy");
+    e = v ? cudaMemcpyAsync(h->v + offset, v, bytes, cudaMemcpyDefault, st)
+          : cudaMemsetAsync(h->v + offset, 0, bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "v copy");
+    return ZERO1_OK;
+}
+
+int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float *master,
+                          float *m, float *v, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (offset > h->n || count > h->n - offset) return fail(ZERO1_EINVAL, "range outside [0, n)");
+    if (count == 0) return ZERO1_OK;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t bytes = count * sizeof(float);
+    cudaError_t e;
+    if (master && (e = cudaMemcpyAsync(master, h->master + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+        return cuda_fail(e, "master copy");
+    if (m && (e = cudaMemcpyAsync(m, h->m + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+        return cuda_fail(e, "m copy");
+    if (v && (e = cudaMemcpyAsync(v, h->v + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+        return cuda_fail(e, "v copy");
+    return ZERO1_OK;
+}
+
+int zero1_set_state(zero1_handle h, const float *master, const float *m, const float *v, uint64_t t, void *stream)
+{
+    int rc = zero1_set_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
+    if (rc) return rc;
+    h->t = t;
+    return ZERO1_OK;
+}
+
+int zero1_get_state(zero1_handle h, float *master, float *m, float *v, uint64_t *t, void *stream)
+{
+    int rc = zero1_get_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
+    if (rc) return rc;
+    if (t) *t = h->t;
+    return ZERO1_OK;
+}
+
+int zero1_set_lr(zero1_handle h, double lr)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!finite_nonneg(lr)) return fail(ZERO1_EINVAL, "lr must be finite and >= 0");
+    h->hp.lr = lr;
+    return ZERO1_OK;
+}
+
+int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    DeviceGuard g(h->device);
+    zero1::DevStatus st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&st, h->status, sizeof st, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (norm) *norm = st.norm;
+    if (clip_coef) *clip_coef = st.clip;
+    return ZERO1_OK;
+}
+
+int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint64_t *device_bytes)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (shard_len) *shard_len = h->shard;
+    if (padded_len) *padded_len = h->padded;
+    if (device_bytes) *device_bytes = h->block_bytes;
+    return ZERO1_OK;
+}
+
+int zero1_profile_start(zero1_handle h, int capacity)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (capacity < 1) return fail(ZERO1_EINVAL, "capacity must be >= 1");
+    DeviceGuard g(h->device);
+    for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
+    h->prof.assign(3 * (size_t)capacity, nullptr);
+    h->prof_capacity = h->prof_used = 0;
+    for (auto &ev : h->prof) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t x : h->prof)
+                if (x) cudaEventDestroy(x);
+            h->prof.clear();
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    h->prof_capacity = capacity;
+    return ZERO1_OK;
+}
+
+int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, uint64_t *steps)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (h->prof_capacity == 0) return fail(ZERO1_EINVAL, "profiling was not started");
+    DeviceGuard g(h->device);
+    double a = 0.0, b = 0.0;
+    cudaError_t e = cudaSuccess;
+    if (h->prof_used > 0) e = cudaEventSynchronize(h->prof[3 * (size_t)h->prof_used - 1]);
+    for (int i = 0; e == cudaSuccess && i < h->prof_used; ++i) {
+        float x = 0.f, y = 0.f;
+        e = cudaEventElapsedTime(&x, h->prof[3 * (size_t)i], h->prof[3 * (size_t)i + 1]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&y, h->prof[3 * (size_t)i + 1], h->prof[3 * (size_t)i + 2]);
+        a += x;
+        b += y;
+    }
+    const uint64_t used = (uint64_t)h->prof_used;
+    for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
+    h->prof.clear();
+    h->prof_capacity = h->prof_used = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "event timing");
+    if (rs_norm_ms) *rs_norm_ms = a;
+    if (update_ms) *update_ms = b;
+    if (steps) *steps = used;
+    return ZERO1_OK;
+}
+
+int zero1_shard_plan(uint64_t n, int world, uint64_t *shard_len, uint64_t *padded_len)
+{
+    if (n == 0) return fail(ZERO1_EINVAL, "n must be > 0");
+    if (world < 1 || world > ZERO1_MAX_WORLD)
+        return fail(ZERO1_EINVAL, "world must be in [1, %d], got %d", ZERO1_MAX_WORLD, world);
+    const uint64_t s = round_up((n + (uint64_t)world - 1) / (uint64_t)world, zero1::kShardAlign);
+    if (shard_len) *shard_len = s;
+    if (padded_len) *padded_len = s * (uint64_t)world;
+    return ZERO1_OK;
+}
+
+int zero1_step_scalars(const zero1_hparams *hp, int world, uint64_t t, float out[8])
+{
+    if (!hp || !out) return fail(ZERO1_EINVAL, "NULL pointer");
+    if (t == 0) return fail(ZERO1_EINVAL, "step numbers start at 1");
+    if (world < 1 || world > ZERO1_MAX_WORLD) return fail(ZERO1_EINVAL, "bad world size %d", world);
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    const zero1::StepScalars s = step_scalars(*hp, world, t);
+    const float v[8] = {s.inv_w, s.beta1, s.omb1, s.beta2, s.omb2, s.step_size, s.decay, s.eps};
+    std::memcpy(out, v, sizeof v);
+    return ZERO1_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// zero1_internal.h -- declarations shared by the C-ABI host code
+// (zero1_host.cu) and the two kernels (zero1_kernels.cu).  Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zero1 {
+
+constexpr int kVec = 8;          // parameters per 16-byte vector of bf16
+constexpr int kThreads = 256;    // threads per CTA, both kernels
+constexpr int kShardAlign = 64;  // shard length multiple (256-byte fp32 shard starts)
+
+// Device-resident result of the norm pass (library-owned, 32 bytes).
+struct DevStatus {
+    double nsq;        // sum of squares of the averaged gradient
+    double norm;       // sqrt(nsq)
+    float clip;        // coefficient the update kernel multiplies into g
+    unsigned ticket;   // last-CTA election counter; 0 between launches
+    unsigned flags;    // bit 0: the norm is not finite
+    unsigned pad;
+};
+constexpr unsigned kFlagNonFinite = 1u;
+
+// Per-step fp32 scalars, formed on the host in double and rounded once.
+struct StepScalars {
+    float inv_w;       // 1/W
+    float beta1, omb1; // beta1, 1 - beta1
+    float beta2, omb2; // beta2, 1 - beta2
+    float step_size;   // lr * sqrt(1 - beta2^t) / (1 - beta1^t)
+    float decay;       // 1 - lr * weight_decay
+    float eps;
+};
+
+// Everything one step's two launches need.
+struct StepLaunch {
+    const void *const *grads;   // W device pointers (bf16, n entries)
+    void *const *params;        // W device pointers (bf16, n entries)
+    int world;
+    uint64_t n;
+    float *master, *m, *v;      // fp32 state, n (padded) entries, 256-B aligned
+    float *ghat;                // fp32 reduce-scatter result, or nullptr: re-read grads
+    double *partials;           // 2 * grid_rs doubles
+    DevStatus *status;
+    StepScalars sc;
+    double max_norm;
+    int grid_rs;                // CTAs of the reduce-scatter + norm kernel
+    int grid_update;            // CTAs of the update + all-gather kernel
+};
+
+// Enqueue the reduce-scatter + norm kernel, then the update + all-gather
+// kernel.  `ev`, when not null, holds three events recorded before, between
+// and after the two kernels.
+cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev);
+
+// Grid sizes: one wave of resident CTAs on this device, capped by the work.
+void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);
+
+}  // namespace zero1
