@@ -186,6 +186,31 @@ int zero1_shard_plan(uint64_t n, int world, uint64_t *shard_len, uint64_t *padde
  * Errors: ZERO1_EINVAL (NULL pointer, t == 0, bad world or hyperparameter). */
 int zero1_step_scalars(const zero1_hparams *hp, int world, uint64_t t, float out[8]);
 
+/* One step that allocates no device memory, for callers that cannot call
+ * cudaMalloc: a framework whose caching allocator has reserved the device's
+ * memory, a plug-in whose host fixes its device memory up front, or a loop
+ * that cannot take the device synchronisation cudaMalloc/cudaFree imply.
+ * The pages have no counterpart to this entry point; it is the same two
+ * kernels as zero1_step with the caller owning all state.
+ *   n, world, hp: as zero1_create; n is limited to 4,194,304 parameters
+ *     (larger n: ZERO1_EINVAL with a message; use zero1_create/zero1_step).
+ *   t: this step's number, 1-based (the caller keeps the count).
+ *   grad_ptrs, param_ptrs: as zero1_step.
+ *   master, m, v: caller-owned device fp32 arrays of n entries, 16-byte
+ *     aligned, updated in place (m = v = 0 before the first step).
+ * Scratch (the fp32 reduce-scatter result, norm partials and status) is a
+ * fixed ~16.1 MiB array inside the library image, held by every GPU that
+ * loads the library until the process exits.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress) with the
+ * device current; make that first call before any stream capture.  Each
+ * call clears the scratch status on `stream` first.  All calls share the
+ * one array: calls whose GPU work overlaps (other streams or threads) race.
+ * The norm is not read back by this call.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ENODEV, ZERO1_ECUDA. */
+int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp, uint64_t t,
+                       const void *const *grad_ptrs, void *const *param_ptrs,
+                       float *master, float *m, float *v, void *stream);
+
 /* Message for the last error on this thread ("" if none). */
 const char *zero1_last_error(void);
 

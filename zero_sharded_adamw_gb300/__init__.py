@@ -22,7 +22,7 @@ __all__ = [
     "zero1_create", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_last_error",
+    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -50,6 +50,7 @@ _SIGS = {
     "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
     "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
+    "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
     "zero1_last_error": (C.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -217,6 +218,15 @@ def zero1_step_scalars(hp: Hparams, world: int, t: int) -> dict:
     _check(_load().zero1_step_scalars(C.byref(c), world, t, out))
     keys = ("inv_w", "beta1", "one_minus_beta1", "beta2", "one_minus_beta2", "step_size", "decay", "eps")
     return dict(zip(keys, list(out)))
+
+
+def zero1_step_noalloc(n: int, world: int, hp: Hparams, t: int, grad_ptrs, param_ptrs,
+                       master, m, v, stream=None) -> None:
+    """One step with caller-owned fp32 state and the library's fixed scratch
+    (no device allocation; n <= 4,194,304)."""
+    c = hp._c()
+    _check(_load().zero1_step_noalloc(n, world, C.byref(c), t, _ptrs(grad_ptrs), _ptrs(param_ptrs),
+                                      _addr(master), _addr(m), _addr(v), _stream(stream)))
 
 
 class Zero1:

@@ -127,6 +127,11 @@ struct DeviceGuard {
 
 }  // namespace
 
+void zero1::set_error_message(const char *msg)
+{
+    snprintf(g_err, sizeof g_err, "%s", msg);
+}
+
 extern "C" {
 
 const char *zero1_last_error(void) { return g_err; }

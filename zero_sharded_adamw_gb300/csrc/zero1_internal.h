@@ -56,4 +56,7 @@ cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *e
 // Grid sizes: one wave of resident CTAs on this device, capped by the work.
 void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);
 
+// Set the message zero1_last_error() returns on this thread.
+void set_error_message(const char *msg);
+
 }  // namespace zero1
