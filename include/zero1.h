@@ -155,7 +155,10 @@ int zero1_set_lr(zero1_handle h, double lr);
 
 /* Norm of the averaged gradient of the latest step and the clip coefficient
  * it applied (1 when not clipped).  Waits for `stream`.  Either output may
- * be NULL.  Before the first step both read 0. */
+ * be NULL.  Before the first step both read 0.  Returns ZERO1_ECUDA if any
+ * step of this handle had a kernel pipeline wait give up (each wait is
+ * bounded to 1 s so that a fault cannot hang the GPU); the state is then not
+ * valid. */
 int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *stream);
 
 /* Layout facts: the shard length S, the padded state length W*S, and the

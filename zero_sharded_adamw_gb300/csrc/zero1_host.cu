@@ -364,6 +364,8 @@ int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *st
     cudaError_t e = cudaMemcpyAsync(&st, h->status, sizeof st, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (st.errors & zero1::kErrWaitTimeout)
+        return fail(ZERO1_ECUDA, "a step kernel's pipeline wait gave up after 1 s; the state is not valid");
     if (norm) *norm = st.norm;
     if (clip_coef) *clip_coef = st.clip;
     return ZERO1_OK;

@@ -17,10 +17,11 @@ struct DevStatus {
     double norm;       // sqrt(nsq)
     float clip;        // coefficient the update kernel multiplies into g
     unsigned ticket;   // last-CTA election counter; 0 between launches
-    unsigned flags;    // bit 0: the norm is not finite
-    unsigned pad;
+    unsigned flags;    // bit 0: the norm is not finite (rewritten every step)
+    unsigned errors;   // sticky: bit 0 = a pipeline wait gave up (1 s limit)
 };
 constexpr unsigned kFlagNonFinite = 1u;
+constexpr unsigned kErrWaitTimeout = 1u;
 
 // Per-step fp32 scalars, formed on the host in double and rounded once.
 struct StepScalars {

@@ -6,7 +6,7 @@
 //                             warp shuffles, one fp64 grid pass by the last
 //                             CTA, which also forms the clip coefficient.
 //  K2  zero1_adamw_ag_kernel  clip scale + AdamW on fp32 master/m/v + bf16
-//                             cast + all-gather (W-way store of each vector).
+//                             cast + all-gather (W-way store of each tile).
 //
 // Sources (web pages, cited by title and section):
 //  "Stanford CS336 Lecture 7 close reading: Parallelism (part 1)", 5.2: the
@@ -18,7 +18,20 @@
 //    correction and decay after it, bf16 copy of the master; "training loop
 //    and checkpoint": clip the concatenated gradient to max_norm.
 //
-// Both kernels are HBM-bound streams (no contraction, so no tensor cores).
+// Both kernels are HBM streams (no contraction, so no tensor cores) built as
+// persistent, warp-specialised TMA pipelines, one CTA per SM:
+//  - a producer warp moves 2048-parameter tiles from HBM into a 4-stage
+//    shared-memory ring with 1-D bulk copies (cp.async.bulk) that complete
+//    on an mbarrier per stage;
+//  - 8 consumer warps (8 parameters per thread per tile) compute out of
+//    shared memory;
+//  - K2 has a store warp whose lanes write the tile's master, m, v and W
+//    bf16 replicas back with bulk stores, so the W-way all-gather costs the
+//    SM one bulk instruction per replica per tile.
+// Every mbarrier wait gives up after 1 s of global time: it raises the CTA's
+// abort flag and a sticky error bit in the status the host reads; a producer
+// that stops lets its loads in flight land before exiting.
+//
 // Every fp32 operation of the sum and the update is an explicit _rn
 // intrinsic: no FMA contraction, IEEE round-to-nearest-even, no FTZ, so the
 // results are those of the plain fp32 definition bit for bit.
@@ -30,30 +43,165 @@
 namespace zero1 {
 namespace {
 
-// ------------------------------------------------------------ memory ops
+constexpr int kTile = 2048;                      // parameters per tile
+constexpr int kStages = 4;                       // shared-memory ring depth
+constexpr int kRankGroup = 8;                    // ranks per K1 stage
+constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kRsThreads = kConsumers + 32;      // + producer warp
+constexpr int kUpdThreads = kConsumers + 64;     // + producer warp + store warp
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+static_assert(kConsumers * kVec == kTile, "one 8-parameter vector per consumer thread");
 
-// 16-byte read-only streaming load: no L1 allocation (each byte is read once
-// per kernel).
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+// ------------------------------------------------------ PTX: TMA, mbarrier
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ float4 ld_stream_f4(const float4 *p)
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
-    float4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-        : "l"(p));
-    return r;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-// Read-write state: plain 16-byte load (the kernel writes the same address).
-__device__ __forceinline__ float4 ld_f4(const float4 *p) { return *p; }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// True once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Global -> shared bulk copy; `bytes` (multiple of 16) are counted on `bar`.
+__device__ __forceinline__ void tma_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void tma_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void tma_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// L2 eviction-priority policies for the cache-hinted copies below.
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_hint(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Shared -> global bulk copy in this thread's current bulk group.
+__device__ __forceinline__ void tma_store_hint(void *gdst, const void *smem_src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+                 "r"(smem_u32(smem_src)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+// 16-byte global store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_hint(float *dst, float4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
+// Drop one 128-byte L2 line without writing it back (dead scratch only).
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Bounded wait on an mbarrier phase.  Gives up when another thread of the
+// CTA has raised `abort`, or after kWaitLimitNs, raising `abort` and the
+// sticky error bit.  Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, DevStatus *status)
+{
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(&status->errors, kErrWaitTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// After an abort, let the producer's last loads land before it exits (the
+// CTA's shared memory must outlive them).  Item k used stage k % kStages,
+// phase (k / kStages) & 1.
+__device__ __forceinline__ void drain_loads(uint64_t *full, uint32_t issued)
+{
+    for (uint32_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k) {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_test(&full[k % kStages], (k / kStages) & 1u) && global_ns() - t0 < kWaitLimitNs) {
+        }
+    }
+}
 
 // ------------------------------------------------------------ bf16 pack
 
@@ -89,8 +237,8 @@ __device__ __forceinline__ unsigned pack2(float lo, float hi)
 // Pointer tables live in the launch parameters (CAP slots, W used).
 template <int CAP>
 struct RsParams {
-    const uint4 *grads[CAP];
-    float4 *ghat;             // nullptr: norm only
+    const uint16_t *grads[CAP];
+    float *ghat;              // nullptr: norm only
     double *partials;         // [2 * gridDim.x]
     DevStatus *status;
     uint64_t nvec;            // n / 8
@@ -102,58 +250,21 @@ struct RsParams {
 
 template <int CAP>
 struct UpdParams {
-    const uint4 *grads[CAP];  // re-read mode only
-    uint4 *params[CAP];
-    const float4 *ghat;       // spill mode only
-    float4 *master, *m, *v;
-    const DevStatus *status;
+    const uint16_t *grads[CAP];  // re-read mode only
+    uint16_t *params[CAP];
+    const float *ghat;           // spill mode only
+    float *master, *m, *v;
+    DevStatus *status;
     uint64_t nvec, n;
     int world;
     StepScalars sc;
 };
 
-// ------------------------------------------------- rank-ordered sum of 8
-
-// s[k] = ((g_0 + g_1) + g_2) + ... + g_{W-1} for the 8 parameters of vector
-// `vec`, in fp32.  W > 0: compile-time world size; W == 0: `world` at run
-// time.  Ranks are loaded in groups of 8 so that a group's loads are all in
-// flight together; the sum itself stays strictly in rank order.
-template <int W>
-__device__ __forceinline__ void rank_sum8(const uint4 *const *grads, int world, uint64_t vec, float s[8])
+// Scalar rank-ordered sum for the last n % 8 parameters.
+__device__ __forceinline__ float rank_sum1(const uint16_t *const *grads, int world, uint64_t e)
 {
-    constexpr int G = 8;
-    const int nw = W > 0 ? W : world;
-    {
-        uint4 raw[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-            if (j < nw) raw[j] = ld_stream(grads[j] + vec);
-        set_widened(s, raw[0]);
-#pragma unroll
-        for (int j = 1; j < G; ++j)
-            if (j < nw) add_widened(s, raw[j]);
-    }
-#pragma unroll 1
-    for (int r0 = G; r0 < nw; r0 += G) {
-        uint4 raw[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-            if (r0 + j < nw) raw[j] = ld_stream(grads[r0 + j] + vec);
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-            if (r0 + j < nw) add_widened(s, raw[j]);
-    }
-}
-
-// Scalar version for the last n % 8 parameters.
-__device__ __forceinline__ float rank_sum1(const uint4 *const *grads, int world, uint64_t e)
-{
-    const unsigned short *g0 = reinterpret_cast<const unsigned short *>(grads[0]);
-    float s = __uint_as_float((unsigned)g0[e] << 16);
-    for (int r = 1; r < world; ++r) {
-        const unsigned short *gr = reinterpret_cast<const unsigned short *>(grads[r]);
-        s = __fadd_rn(s, __uint_as_float((unsigned)gr[e] << 16));
-    }
+    float s = __uint_as_float((unsigned)grads[0][e] << 16);
+    for (int r = 1; r < world; ++r) s = __fadd_rn(s, __uint_as_float((unsigned)grads[r][e] << 16));
     return s;
 }
 
@@ -182,10 +293,10 @@ __device__ __forceinline__ float sumsq8(const float g[8])
                      __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
 }
 
-// Fixed-order block sum of two doubles (warp shuffle tree, then warp 0).
-__device__ __forceinline__ void block_sum2(double &a, double &b)
+// Fixed-order sum of two doubles over the consumer threads (warp shuffle
+// tree, then warp 0); the result is valid in consumer thread 0.
+__device__ __forceinline__ void consumer_sum2(double &a, double &b, double *sa, double *sb)
 {
-    __shared__ double sa[kThreads / 32], sb[kThreads / 32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         a += __shfl_down_sync(0xFFFFFFFFu, a, off);
@@ -196,70 +307,161 @@ __device__ __forceinline__ void block_sum2(double &a, double &b)
         sa[warp] = a;
         sb[warp] = b;
     }
-    __syncthreads();
+    consumer_sync();
     if (warp == 0) {
-        a = lane < kThreads / 32 ? sa[lane] : 0.0;
-        b = lane < kThreads / 32 ? sb[lane] : 0.0;
+        a = lane < kConsumerWarps ? sa[lane] : 0.0;
+        b = lane < kConsumerWarps ? sb[lane] : 0.0;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             a += __shfl_down_sync(0xFFFFFFFFu, a, off);
             b += __shfl_down_sync(0xFFFFFFFFu, b, off);
         }
     }
-    __syncthreads();
+    consumer_sync();
 }
 
 // ------------------------------------------------------------------- K1
 
+struct RsSmem {
+    uint16_t g[kStages][kRankGroup][kTile];   // 128 KB: one rank group of one tile per stage
+    uint64_t full[kStages], empty[kStages];
+    double red_a[kConsumerWarps], red_b[kConsumerWarps];
+    int abort;
+    int last;
+};
+
+// Warps 0..7 consume, warp 8 produces.  Work item k of a CTA is (tile j,
+// rank group grp), tiles j = blockIdx.x, +gridDim.x, ... in increasing order
+// and, within a tile, rank groups in increasing order, so each consumer
+// thread's fp32 sum runs over the ranks strictly in order 0..W-1.
 template <int W, int CAP, bool SPILL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kRsThreads, 1)
 zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 {
-    Kahan acc;
-    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
-    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-    for (uint64_t vec = tid; vec < p.nvec; vec += stride) {
-        float s[8];
-        rank_sum8<W>(p.grads, p.world, vec, s);
-        float g[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) g[k] = __fmul_rn(s[k], p.inv_w);
-        if (SPILL) {
-            p.ghat[2 * vec] = make_float4(g[0], g[1], g[2], g[3]);
-            p.ghat[2 * vec + 1] = make_float4(g[4], g[5], g[6], g[7]);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    RsSmem &sm = *reinterpret_cast<RsSmem *>(smem_raw);
+    const int nw = W > 0 ? W : p.world;
+    const int ngroups = (nw + kRankGroup - 1) / kRankGroup;
+    const uint64_t nel = p.nvec * kVec;
+    const uint64_t ntiles = (nel + kTile - 1) / kTile;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
         }
-        acc.add(sumsq8(g));
+        sm.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // The last n % 8 parameters, one per thread of the first CTA.
-    const uint64_t e = p.nvec * kVec + tid;
-    if (tid < kVec && e < p.n) {
-        float g = __fmul_rn(rank_sum1(p.grads, p.world, e), p.inv_w);
-        if (SPILL) reinterpret_cast<float *>(p.ghat)[e] = g;
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {                                 // producer
+        if (lane == 0) {
+            // With a scratch ĝ, gradients go first out of L2 so that the ĝ
+            // written last stays resident for the update kernel; when the
+            // update kernel re-reads the gradients they keep normal priority.
+            const uint64_t pol = SPILL ? policy_evict_first() : 0;
+            uint32_t k = 0;
+            for (uint64_t j = blockIdx.x; j < ntiles && !*abort; j += gridDim.x) {
+                const uint64_t base = j * kTile;
+                const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+                for (int grp = 0; grp < ngroups; ++grp, ++k) {
+                    const int s = k % kStages;
+                    if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, p.status))
+                        break;
+                    const int r0 = grp * kRankGroup;
+                    const int rn = nw - r0 < kRankGroup ? nw - r0 : kRankGroup;
+                    mbar_arrive_expect_tx(&sm.full[s], (uint32_t)rn * cnt * 2u);
+                    for (int r = 0; r < rn; ++r) {
+                        if (SPILL)
+                            tma_load_hint(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
+                        else
+                            tma_load(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
+                    }
+                }
+            }
+            if (*abort) drain_loads(sm.full, k);
+        }
+        return;
+    }
+
+    // Consumers: thread t owns parameters [8t, 8t+8) of every tile.
+    Kahan acc;
+    const uint64_t keep = policy_evict_last();
+    const uint32_t e0 = threadIdx.x * kVec;
+    uint32_t k = 0;
+    for (uint64_t j = blockIdx.x; j < ntiles; j += gridDim.x) {
+        if (__any_sync(0xFFFFFFFFu, *abort != 0)) break;
+        const uint64_t base = j * kTile;
+        const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+        const bool act = e0 < cnt;
+        float s[8];
+        bool ok = true;
+        for (int grp = 0; grp < ngroups; ++grp, ++k) {
+            const int st = k % kStages;
+            const bool got = mbar_wait(&sm.full[st], (k / kStages) & 1u, abort, p.status);
+            if (!__all_sync(0xFFFFFFFFu, got)) {      // warp-uniform: no lane left behind
+                ok = false;
+                break;
+            }
+            const int rn = nw - grp * kRankGroup < kRankGroup ? nw - grp * kRankGroup : kRankGroup;
+            if (act) {
+#pragma unroll
+                for (int r = 0; r < kRankGroup; ++r) {
+                    if (r < rn) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][r][e0]);
+                        if (grp == 0 && r == 0)
+                            set_widened(s, raw);
+                        else
+                            add_widened(s, raw);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[st]);
+        }
+        if (!ok) break;
+        if (act) {
+            float g[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(s[q], p.inv_w);
+            if (SPILL) {
+                st_hint(p.ghat + base + e0, make_float4(g[0], g[1], g[2], g[3]), keep);
+                st_hint(p.ghat + base + e0 + 4, make_float4(g[4], g[5], g[6], g[7]), keep);
+            }
+            acc.add(sumsq8(g));
+        }
+    }
+    // The last n % 8 parameters, one per thread of CTA 0.
+    const uint64_t e = nel + threadIdx.x;
+    if (blockIdx.x == 0 && threadIdx.x < kVec && e < p.n) {
+        const float g = __fmul_rn(rank_sum1(p.grads, nw, e), p.inv_w);
+        if (SPILL) p.ghat[e] = g;
         acc.add(__fmul_rn(g, g));
     }
 
     double a = (double)acc.hi - (double)acc.lo;
     double b = (double)acc.plain;
-    block_sum2(a, b);
-
-    __shared__ bool last;
+    consumer_sum2(a, b, sm.red_a, sm.red_b);
     if (threadIdx.x == 0) {
         p.partials[blockIdx.x] = a;
         p.partials[gridDim.x + blockIdx.x] = b;
         __threadfence();
-        last = atomicAdd(&p.status->ticket, 1u) == gridDim.x - 1;
+        sm.last = atomicAdd(&p.status->ticket, 1u) == gridDim.x - 1;
     }
-    __syncthreads();
-    if (!last) return;
+    consumer_sync();
+    if (!sm.last) return;
 
     // Last CTA: sum the per-CTA partials in a fixed order (deterministic).
     __threadfence();
     double x = 0.0, y = 0.0;
-    for (unsigned i = threadIdx.x; i < gridDim.x; i += kThreads) {
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += kConsumers) {
         x += __ldcg(p.partials + i);
         y += __ldcg(p.partials + gridDim.x + i);
     }
-    block_sum2(x, y);
+    consumer_sum2(x, y, sm.red_a, sm.red_b);
     if (threadIdx.x == 0) {
         const double nsq = isfinite(y) ? x : y;
         const double norm = sqrt(nsq);
@@ -281,8 +483,7 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 // ------------------------------------------------------------------- K2
 
 // One parameter of the AdamW update, in the order the update is written.
-__device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s,
-                                       float &master, float &m, float &v)
+__device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, float &master, float &m, float &v)
 {
     const float g = __fmul_rn(gh, c);
     const float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, g));
@@ -296,120 +497,230 @@ __device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s,
     v = vi;
 }
 
+struct UpdSmem {
+    float in[kStages][4][kTile];   // 128 KB: ghat (or the W <= 2 bf16 grads), master, m, v
+    uint16_t b16[kStages][kTile];  // 16 KB: the tile's bf16 parameters
+    uint64_t full[kStages], done[kStages], empty[kStages];
+    int abort;
+};
+
+// Four consecutive parameters at offset o of stage s: AdamW in place on the
+// staged master, m, v and the bf16 values into the replica tile.
+template <bool REREAD>
+__device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc)
+{
+    float gh[4];
+    if (REREAD) {
+        const uint16_t *g = reinterpret_cast<const uint16_t *>(sm.in[s][0]);
+        uint2 raw = *reinterpret_cast<const uint2 *>(g + o);
+        gh[0] = __uint_as_float(raw.x << 16);
+        gh[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+        gh[2] = __uint_as_float(raw.y << 16);
+        gh[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        for (int r = 1; r < nw; ++r) {
+            raw = *reinterpret_cast<const uint2 *>(g + r * kTile + o);
+            gh[0] = __fadd_rn(gh[0], __uint_as_float(raw.x << 16));
+            gh[1] = __fadd_rn(gh[1], __uint_as_float(raw.x & 0xFFFF0000u));
+            gh[2] = __fadd_rn(gh[2], __uint_as_float(raw.y << 16));
+            gh[3] = __fadd_rn(gh[3], __uint_as_float(raw.y & 0xFFFF0000u));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) gh[q] = __fmul_rn(gh[q], sc.inv_w);
+    } else {
+        const float4 a = *reinterpret_cast<const float4 *>(&sm.in[s][0][o]);
+        gh[0] = a.x;
+        gh[1] = a.y;
+        gh[2] = a.z;
+        gh[3] = a.w;
+    }
+    float4 *w4 = reinterpret_cast<float4 *>(&sm.in[s][1][o]);
+    float4 *m4 = reinterpret_cast<float4 *>(&sm.in[s][2][o]);
+    float4 *v4 = reinterpret_cast<float4 *>(&sm.in[s][3][o]);
+    float4 w = *w4, m = *m4, v = *v4;
+    adamw1(gh[0], c, sc, w.x, m.x, v.x);
+    adamw1(gh[1], c, sc, w.y, m.y, v.y);
+    adamw1(gh[2], c, sc, w.z, m.z, v.z);
+    adamw1(gh[3], c, sc, w.w, m.w, v.w);
+    *w4 = w;
+    *m4 = m;
+    *v4 = v;
+    *reinterpret_cast<uint2 *>(&sm.b16[s][o]) = make_uint2(pack2(w.x, w.y), pack2(w.z, w.w));
+}
+
+// Warps 0..7 consume, warp 8 produces, warp 9 stores.  Tiles are walked
+// from the highest down (the reduce-scatter kernel wrote those last, so
+// they are the likeliest to still be in L2).  master, m, v are updated in
+// place in the stage and written back from there.
 template <int W, int CAP, bool REREAD>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kUpdThreads, 1)
 zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 {
-    const float c = p.status->clip;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    UpdSmem &sm = *reinterpret_cast<UpdSmem *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
-    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
-    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (tid < p.nvec) {
-        // Walk this thread's vectors from the highest address down: the
-        // reduce-scatter kernel wrote those last, so they are the likeliest
-        // to still sit in L2.
-        uint64_t k = (p.nvec - 1 - tid) / stride;
-        for (;;) {
-            const uint64_t vec = tid + k * stride;
-            float gh[8];
-            if (REREAD) {
-                rank_sum8<W>(p.grads, p.world, vec, gh);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gh[j] = __fmul_rn(gh[j], p.sc.inv_w);
-            } else {
-                const float4 a = ld_stream_f4(p.ghat + 2 * vec);
-                const float4 b = ld_stream_f4(p.ghat + 2 * vec + 1);
-                gh[0] = a.x; gh[1] = a.y; gh[2] = a.z; gh[3] = a.w;
-                gh[4] = b.x; gh[5] = b.y; gh[6] = b.z; gh[7] = b.w;
-            }
-            float4 w0 = ld_f4(p.master + 2 * vec), w1 = ld_f4(p.master + 2 * vec + 1);
-            float4 m0 = ld_f4(p.m + 2 * vec), m1 = ld_f4(p.m + 2 * vec + 1);
-            float4 v0 = ld_f4(p.v + 2 * vec), v1 = ld_f4(p.v + 2 * vec + 1);
-            adamw1(gh[0], c, p.sc, w0.x, m0.x, v0.x);
-            adamw1(gh[1], c, p.sc, w0.y, m0.y, v0.y);
-            adamw1(gh[2], c, p.sc, w0.z, m0.z, v0.z);
-            adamw1(gh[3], c, p.sc, w0.w, m0.w, v0.w);
-            adamw1(gh[4], c, p.sc, w1.x, m1.x, v1.x);
-            adamw1(gh[5], c, p.sc, w1.y, m1.y, v1.y);
-            adamw1(gh[6], c, p.sc, w1.z, m1.z, v1.z);
-            adamw1(gh[7], c, p.sc, w1.w, m1.w, v1.w);
-            p.master[2 * vec] = w0; p.master[2 * vec + 1] = w1;
-            p.m[2 * vec] = m0;      p.m[2 * vec + 1] = m1;
-            p.v[2 * vec] = v0;      p.v[2 * vec + 1] = v1;
-            const uint4 b16 = make_uint4(pack2(w0.x, w0.y), pack2(w0.z, w0.w),
-                                         pack2(w1.x, w1.y), pack2(w1.z, w1.w));
-            // All-gather: every rank's replica receives the same 16 bytes.
-#pragma unroll 8
-            for (int r = 0; r < nw; ++r) __stcs(p.params[r] + vec, b16);
-            if (k == 0) break;
-            --k;
+    const uint64_t nel = p.nvec * kVec;
+    const int64_t ntiles = (int64_t)((nel + kTile - 1) / kTile);
+    const int64_t first = ntiles - 1 - (int64_t)blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.done[s], kConsumerWarps);
+            mbar_init(&sm.empty[s], 1);
         }
+        sm.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    const uint64_t e = p.nvec * kVec + tid;
-    if (tid < kVec && e < p.n) {
-        float gh;
-        if (REREAD)
-            gh = __fmul_rn(rank_sum1(p.grads, p.world, e), p.sc.inv_w);
-        else
-            gh = reinterpret_cast<const float *>(p.ghat)[e];
-        float *mw = reinterpret_cast<float *>(p.master);
-        float *mm = reinterpret_cast<float *>(p.m);
-        float *mv = reinterpret_cast<float *>(p.v);
-        float w = mw[e], m = mm[e], v = mv[e];
+    __syncthreads();
+
+    // Every byte this kernel moves is touched once per step: lowest L2 priority.
+    const uint64_t once = policy_evict_first();
+
+    if (warp == kConsumerWarps) {                                 // producer
+        if (lane == 0) {
+            uint32_t k = 0;
+            for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
+                const int s = k % kStages;
+                if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, p.status)) break;
+                const uint64_t base = (uint64_t)j * kTile;
+                const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+                const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
+                mbar_arrive_expect_tx(&sm.full[s], gbytes + 12u * cnt);
+                if (REREAD) {
+                    uint16_t *g = reinterpret_cast<uint16_t *>(sm.in[s][0]);
+                    for (int r = 0; r < nw; ++r)
+                        tma_load_hint(g + r * kTile, p.grads[r] + base, cnt * 2u, &sm.full[s], once);
+                } else {
+                    tma_load_hint(sm.in[s][0], p.ghat + base, cnt * 4u, &sm.full[s], once);
+                }
+                tma_load_hint(sm.in[s][1], p.master + base, cnt * 4u, &sm.full[s], once);
+                tma_load_hint(sm.in[s][2], p.m + base, cnt * 4u, &sm.full[s], once);
+                tma_load_hint(sm.in[s][3], p.v + base, cnt * 4u, &sm.full[s], once);
+            }
+            if (*abort) drain_loads(sm.full, k);
+        }
+        return;
+    }
+
+    if (warp == kConsumerWarps + 1) {                             // stores
+        uint32_t k = 0;
+        for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
+            const int s = k % kStages;
+            const bool got = mbar_wait(&sm.done[s], (k / kStages) & 1u, abort, p.status);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            const uint64_t base = (uint64_t)j * kTile;
+            const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+            // Targets 0..2 are master, m, v; 3.. are the W replicas (the
+            // all-gather).  Lane L issues targets L, L+32, ...
+            for (int t = lane; t < nw + 3; t += 32) {
+                if (t < 3) {
+                    float *dst = t == 0 ? p.master : t == 1 ? p.m : p.v;
+                    tma_store_hint(dst + base, sm.in[s][1 + t], cnt * 4u, once);
+                } else {
+                    tma_store_hint(p.params[t - 3] + base, sm.b16[s], cnt * 2u, once);
+                }
+            }
+            tma_commit();
+            if (k >= 1) {                      // the previous tile's stores have read its stage
+                tma_wait_read<1>();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.empty[(k - 1) % kStages]);
+            }
+        }
+        tma_wait_all();
+        return;
+    }
+
+    // Consumers: thread t owns parameters [4t, 4t+4) and [1024+4t, 1024+4t+4)
+    // of every tile, so a warp's 16-byte shared-memory accesses are
+    // consecutive (no bank conflicts).
+    const float c = p.status->clip;
+    const uint32_t o0 = threadIdx.x * 4u, o1 = kTile / 2 + threadIdx.x * 4u;
+    uint32_t k = 0;
+    for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
+        const int s = k % kStages;
+        const bool got = mbar_wait(&sm.full[s], (k / kStages) & 1u, abort, p.status);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        const uint64_t base = (uint64_t)j * kTile;
+        const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+        if (!REREAD && threadIdx.x < cnt / 32u) {
+            // This tile's ĝ is in shared memory now and dead in HBM: drop its
+            // whole 128-byte lines from L2 unwritten (a partly covered last
+            // line may hold the n % 8 tail and is left alone).
+            discard_l2_line(p.ghat + base + threadIdx.x * 32u);
+        }
+        if (o0 < cnt) update4<REREAD>(sm, s, o0, nw, c, p.sc);
+        if (o1 < cnt) update4<REREAD>(sm, s, o1, nw, c, p.sc);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.done[s]);
+    }
+
+    // The last n % 8 parameters, one per thread of CTA 0, straight from HBM.
+    const uint64_t e = nel + threadIdx.x;
+    if (blockIdx.x == 0 && threadIdx.x < kVec && e < p.n) {
+        const float gh = REREAD ? __fmul_rn(rank_sum1(p.grads, nw, e), p.sc.inv_w) : p.ghat[e];
+        float w = p.master[e], m = p.m[e], v = p.v[e];
         adamw1(gh, c, p.sc, w, m, v);
-        mw[e] = w;
-        mm[e] = m;
-        mv[e] = v;
-        const __nv_bfloat16 b = __float2bfloat16_rn(w);
-        for (int r = 0; r < nw; ++r)
-            reinterpret_cast<__nv_bfloat16 *>(p.params[r])[e] = b;
+        p.master[e] = w;
+        p.m[e] = m;
+        p.v[e] = v;
+        const __nv_bfloat16 bw = __float2bfloat16_rn(w);
+        for (int r = 0; r < nw; ++r) reinterpret_cast<__nv_bfloat16 *>(p.params[r])[e] = bw;
     }
 }
 
 // ------------------------------------------------------------- launchers
 
+template <typename Kernel>
+cudaError_t allow_smem(Kernel kernel, size_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 template <int W, int CAP>
 cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
 {
-    const uint64_t nvec = s.n / kVec;
     RsParams<CAP> rp{};
     UpdParams<CAP> up{};
     for (int r = 0; r < s.world; ++r) {
-        rp.grads[r] = static_cast<const uint4 *>(s.grads[r]);
-        up.grads[r] = static_cast<const uint4 *>(s.grads[r]);
-        up.params[r] = static_cast<uint4 *>(s.params[r]);
+        rp.grads[r] = static_cast<const uint16_t *>(s.grads[r]);
+        up.grads[r] = static_cast<const uint16_t *>(s.grads[r]);
+        up.params[r] = static_cast<uint16_t *>(s.params[r]);
     }
-    rp.ghat = reinterpret_cast<float4 *>(s.ghat);
+    rp.ghat = s.ghat;
     rp.partials = s.partials;
     rp.status = s.status;
-    rp.nvec = nvec;
+    rp.nvec = s.n / kVec;
     rp.n = s.n;
     rp.world = s.world;
     rp.inv_w = s.sc.inv_w;
     rp.max_norm = s.max_norm;
 
-    up.ghat = reinterpret_cast<const float4 *>(s.ghat);
-    up.master = reinterpret_cast<float4 *>(s.master);
-    up.m = reinterpret_cast<float4 *>(s.m);
-    up.v = reinterpret_cast<float4 *>(s.v);
+    up.ghat = s.ghat;
+    up.master = s.master;
+    up.m = s.m;
+    up.v = s.v;
     up.status = s.status;
-    up.nvec = nvec;
+    up.nvec = s.n / kVec;
     up.n = s.n;
     up.world = s.world;
     up.sc = s.sc;
 
+    const bool spill = s.ghat != nullptr;
+    if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
+    auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
+    auto k2 = spill ? zero1_adamw_ag_kernel<W, CAP, false> : zero1_adamw_ag_kernel<W, CAP, true>;
     cudaError_t e;
+    if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
+    if ((e = allow_smem(k2, sizeof(UpdSmem))) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    if (s.ghat)
-        zero1_rs_norm_kernel<W, CAP, true><<<s.grid_rs, kThreads, 0, stream>>>(rp);
-    else
-        zero1_rs_norm_kernel<W, CAP, false><<<s.grid_rs, kThreads, 0, stream>>>(rp);
+    k1<<<s.grid_rs, kRsThreads, sizeof(RsSmem), stream>>>(rp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-    if (s.ghat)
-        zero1_adamw_ag_kernel<W, CAP, false><<<s.grid_update, kThreads, 0, stream>>>(up);
-    else
-        zero1_adamw_ag_kernel<W, CAP, true><<<s.grid_update, kThreads, 0, stream>>>(up);
+    k2<<<s.grid_update, kUpdThreads, sizeof(UpdSmem), stream>>>(up);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -438,13 +749,11 @@ void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, i
 {
     (void)world;
     (void)reread;
-    // 256-thread CTAs; 4 resident per SM keeps ~64 KB of loads in flight per
-    // SM for the 16-byte streams, and both kernels fit that at their register
-    // budgets.  Never more CTAs than there are vectors to process.
-    const uint64_t nvec = n / kVec;
-    const uint64_t need = (nvec + kThreads - 1) / kThreads;
-    uint64_t g = (uint64_t)num_sms * 4;
-    if (need < g) g = need;
+    // Persistent kernels: one CTA per SM (each holds ~130-150 KB of shared
+    // memory), never more CTAs than tiles, at least one (the n % 8 tail).
+    const uint64_t ntiles = (n / kVec * kVec + kTile - 1) / kTile;
+    uint64_t g = (uint64_t)num_sms;
+    if (ntiles < g) g = ntiles;
     if (g < 1) g = 1;
     *grid_rs = (int)g;
     *grid_update = (int)g;
