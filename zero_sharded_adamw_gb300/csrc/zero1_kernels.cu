@@ -322,18 +322,27 @@ __device__ __forceinline__ void consumer_sum2(double &a, double &b, double *sa, 
 
 // ------------------------------------------------------------------- K1
 
+// Parameters of tile j that lie in the 8-aligned vector part [0, nel).
+__device__ __forceinline__ uint32_t tile_count(uint64_t nel, uint64_t j)
+{
+    const uint64_t base = j * kTile;
+    return (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+}
+
 struct RsSmem {
-    uint16_t g[kStages][kRankGroup][kTile];   // 128 KB: one rank group of one tile per stage
+    uint16_t g[kStages][kRankGroup][kTile];   // 128 KB: eight 4 KB (rank, tile) slices per stage
     uint64_t full[kStages], empty[kStages];
     double red_a[kConsumerWarps], red_b[kConsumerWarps];
     int abort;
     int last;
 };
 
-// Warps 0..7 consume, warp 8 produces.  Work item k of a CTA is (tile j,
-// rank group grp), tiles j = blockIdx.x, +gridDim.x, ... in increasing order
-// and, within a tile, rank groups in increasing order, so each consumer
-// thread's fp32 sum runs over the ranks strictly in order 0..W-1.
+// Warps 0..7 consume, warp 8 produces.  A CTA's tiles are j = blockIdx.x,
+// +gridDim.x, ... in increasing order; work item k of a CTA is (batch b,
+// rank group grp): for W >= 8 a batch is one tile and its rank groups come
+// in increasing order, for W < 8 a batch is `sub` consecutive tiles of the
+// CTA with all ranks.  Either way each consumer thread's fp32 sum runs over
+// the ranks strictly in order 0..W-1.
 template <int W, int CAP, bool SPILL>
 __global__ void __launch_bounds__(kRsThreads, 1)
 zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
@@ -341,9 +350,15 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     RsSmem &sm = *reinterpret_cast<RsSmem *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
+    // A stage holds eight 4 KB (rank, tile) slices: one rank group of one
+    // tile when W >= 8, else `sub` whole tiles of all W ranks.
     const int ngroups = (nw + kRankGroup - 1) / kRankGroup;
+    const int sub = nw >= kRankGroup ? 1 : kRankGroup / nw;
     const uint64_t nel = p.nvec * kVec;
     const uint64_t ntiles = (nel + kTile - 1) / kTile;
+    // This CTA's tiles: blockIdx.x + i * gridDim.x for i < tcta.
+    const uint32_t tcta = blockIdx.x < ntiles ? (uint32_t)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    auto tile_of = [&](uint32_t i) -> uint64_t { return blockIdx.x + (uint64_t)i * gridDim.x; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
 
@@ -364,21 +379,26 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
             // update kernel re-reads the gradients they keep normal priority.
             const uint64_t pol = SPILL ? policy_evict_first() : 0;
             uint32_t k = 0;
-            for (uint64_t j = blockIdx.x; j < ntiles && !*abort; j += gridDim.x) {
-                const uint64_t base = j * kTile;
-                const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+            for (uint32_t b = 0; b * sub < tcta && !*abort; ++b) {
                 for (int grp = 0; grp < ngroups; ++grp, ++k) {
                     const int s = k % kStages;
                     if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, p.status))
                         break;
                     const int r0 = grp * kRankGroup;
                     const int rn = nw - r0 < kRankGroup ? nw - r0 : kRankGroup;
-                    mbar_arrive_expect_tx(&sm.full[s], (uint32_t)rn * cnt * 2u);
-                    for (int r = 0; r < rn; ++r) {
-                        if (SPILL)
-                            tma_load_hint(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
-                        else
-                            tma_load(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
+                    uint32_t bytes = 0;
+                    for (int q = 0; q < sub && b * sub + q < tcta; ++q)
+                        bytes += (uint32_t)rn * tile_count(nel, tile_of(b * sub + q)) * 2u;
+                    mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
+                        const uint64_t base = tile_of(b * sub + q) * kTile;
+                        const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
+                        for (int r = 0; r < rn; ++r) {
+                            if (SPILL)
+                                tma_load_hint(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
+                            else
+                                tma_load(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
+                        }
                     }
                 }
             }
@@ -392,12 +412,9 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
     const uint64_t keep = policy_evict_last();
     const uint32_t e0 = threadIdx.x * kVec;
     uint32_t k = 0;
-    for (uint64_t j = blockIdx.x; j < ntiles; j += gridDim.x) {
+    float s[8];
+    for (uint32_t b = 0; b * sub < tcta; ++b) {
         if (__any_sync(0xFFFFFFFFu, *abort != 0)) break;
-        const uint64_t base = j * kTile;
-        const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
-        const bool act = e0 < cnt;
-        float s[8];
         bool ok = true;
         for (int grp = 0; grp < ngroups; ++grp, ++k) {
             const int st = k % kStages;
@@ -407,15 +424,29 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
                 break;
             }
             const int rn = nw - grp * kRankGroup < kRankGroup ? nw - grp * kRankGroup : kRankGroup;
-            if (act) {
+            for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
+                const uint64_t base = tile_of(b * sub + q) * kTile;
+                const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
+                if (e0 < cnt) {
 #pragma unroll
-                for (int r = 0; r < kRankGroup; ++r) {
-                    if (r < rn) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][r][e0]);
-                        if (grp == 0 && r == 0)
-                            set_widened(s, raw);
-                        else
-                            add_widened(s, raw);
+                    for (int r = 0; r < kRankGroup; ++r) {
+                        if (r < rn) {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][q * rn + r][e0]);
+                            if (grp == 0 && r == 0)
+                                set_widened(s, raw);
+                            else
+                                add_widened(s, raw);
+                        }
+                    }
+                    if (grp == ngroups - 1) {          // all W ranks summed: finish the tile
+                        float g[8];
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) g[c8] = __fmul_rn(s[c8], p.inv_w);
+                        if (SPILL) {
+                            st_hint(p.ghat + base + e0, make_float4(g[0], g[1], g[2], g[3]), keep);
+                            st_hint(p.ghat + base + e0 + 4, make_float4(g[4], g[5], g[6], g[7]), keep);
+                        }
+                        acc.add(sumsq8(g));
                     }
                 }
             }
@@ -423,16 +454,6 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
             if (lane == 0) mbar_arrive(&sm.empty[st]);
         }
         if (!ok) break;
-        if (act) {
-            float g[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(s[q], p.inv_w);
-            if (SPILL) {
-                st_hint(p.ghat + base + e0, make_float4(g[0], g[1], g[2], g[3]), keep);
-                st_hint(p.ghat + base + e0 + 4, make_float4(g[4], g[5], g[6], g[7]), keep);
-            }
-            acc.add(sumsq8(g));
-        }
     }
     // The last n % 8 parameters, one per thread of CTA 0.
     const uint64_t e = nel + threadIdx.x;
