@@ -120,8 +120,11 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
  * zero1_step, copies the W replicas back, and waits for the stream.
  *   host_grads:  W host pointers, n bf16 each (pinned memory recommended).
  *   host_params: W host pointers, n bf16 each, written.
- * The first call allocates the staging buffers (4*W*n bytes, freed by
- * zero1_destroy).  Errors as zero1_step, plus ZERO1_ENOMEM. */
+ * The copies are cut into chunks of at most 64 MiB spread over four internal
+ * copy streams (ordered after earlier work on `stream`, and `stream` waits
+ * for them), so that several copy engines run at once.  The first call
+ * allocates the staging buffers (4*W*n bytes) and creates those streams;
+ * zero1_destroy frees both.  Errors as zero1_step, plus ZERO1_ENOMEM. */
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
 
 /* Checkpoint restore ("Parallel training", "training loop and checkpoint":

@@ -41,9 +41,13 @@ struct zero1_ctx {
     float *master = nullptr, *m = nullptr, *v = nullptr, *ghat = nullptr;
     double *partials = nullptr;
     zero1::DevStatus *status = nullptr;
-    // host-path staging (zero1_step_host), allocated on first use
+    // host-path staging (zero1_step_host), allocated on first use, and the
+    // copy streams its host<->device copies are spread over
     void *staging = nullptr;
     uint64_t staging_stride = 0;
+    bool copy_ready = false;
+    cudaStream_t copy_stream[4] = {};
+    cudaEvent_t copy_fork = nullptr, copy_join[4] = {};
     // per-kernel timing (zero1_profile_start/stop): 3 events per step
     std::vector<cudaEvent_t> prof;
     int prof_capacity = 0, prof_used = 0;
@@ -214,6 +218,13 @@ int zero1_destroy(zero1_handle h)
     cudaError_t e2 = cudaFree(h->block);
     cudaError_t e3 = h->staging ? cudaFree(h->staging) : cudaSuccess;
     for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
+    if (h->copy_ready) {
+        for (int i = 0; i < 4; ++i) {
+            cudaStreamDestroy(h->copy_stream[i]);
+            cudaEventDestroy(h->copy_join[i]);
+        }
+        cudaEventDestroy(h->copy_fork);
+    }
     delete h;
     if (e1 != cudaSuccess) return cuda_fail(e1, "cudaDeviceSynchronize in destroy");
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
@@ -255,6 +266,55 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     return ZERO1_OK;
 }
 
+namespace {
+
+constexpr int kCopyStreams = 4;
+constexpr uint64_t kCopyChunk = 64ull << 20;
+
+// `count` copies of `bytes` each, cut into chunks of at most 64 MiB and dealt
+// round-robin over the handle's copy streams so that several copy engines
+// run at once; they start after the work already on `st` and the work
+// enqueued on `st` afterwards waits for all of them.
+int spread_copies(zero1_ctx *h, void *const *dst, const void *const *src, int count, uint64_t bytes,
+                  cudaMemcpyKind kind, cudaStream_t st)
+{
+    cudaError_t e;
+    if (!h->copy_ready) {
+        for (int i = 0; i < kCopyStreams; ++i) {
+            if ((e = cudaStreamCreateWithFlags(&h->copy_stream[i], cudaStreamNonBlocking)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamCreate");
+            if ((e = cudaEventCreateWithFlags(&h->copy_join[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "cudaEventCreate");
+        }
+        if ((e = cudaEventCreateWithFlags(&h->copy_fork, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreate");
+        h->copy_ready = true;
+    }
+    if ((e = cudaEventRecord(h->copy_fork, st)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    for (int i = 0; i < kCopyStreams; ++i)
+        if ((e = cudaStreamWaitEvent(h->copy_stream[i], h->copy_fork, 0)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamWaitEvent");
+    int next = 0;
+    for (int r = 0; r < count; ++r) {
+        for (uint64_t off = 0; off < bytes; off += kCopyChunk) {
+            const uint64_t len = bytes - off < kCopyChunk ? bytes - off : kCopyChunk;
+            e = cudaMemcpyAsync(static_cast<char *>(dst[r]) + off, static_cast<const char *>(src[r]) + off, len,
+                                kind, h->copy_stream[next]);
+            if (e != cudaSuccess) return cuda_fail(e, "host/device copy");
+            next = (next + 1) % kCopyStreams;
+        }
+    }
+    for (int i = 0; i < kCopyStreams; ++i) {
+        if ((e = cudaEventRecord(h->copy_join[i], h->copy_stream[i])) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(st, h->copy_join[i], 0)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    return ZERO1_OK;
+}
+
+}  // namespace
+
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
@@ -272,20 +332,19 @@ int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *
             return cuda_fail(e, "cudaMalloc of staging buffers");
         }
     }
-    const void *dg[ZERO1_MAX_WORLD];
+    void *dg[ZERO1_MAX_WORLD];
     void *dp[ZERO1_MAX_WORLD];
     char *base = static_cast<char *>(h->staging);
     for (int r = 0; r < h->world; ++r) {
         dg[r] = base + (uint64_t)r * h->staging_stride;
         dp[r] = base + (uint64_t)(h->world + r) * h->staging_stride;
-        if ((e = cudaMemcpyAsync(const_cast<void *>(dg[r]), host_grads[r], bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return cuda_fail(e, "host-to-device gradient copy");
     }
-    int rc = zero1_step(h, dg, dp, stream);
+    int rc = spread_copies(h, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st);
     if (rc) return rc;
-    for (int r = 0; r < h->world; ++r)
-        if ((e = cudaMemcpyAsync(host_params[r], dp[r], bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-            return cuda_fail(e, "device-to-host replica copy");
+    rc = zero1_step(h, dg, dp, stream);
+    if (rc) return rc;
+    rc = spread_copies(h, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st);
+    if (rc) return rc;
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return ZERO1_OK;
 }
