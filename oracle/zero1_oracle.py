@@ -70,6 +70,8 @@ def _signatures():
         "zref_step": (None, [u64, i32, P, u64, P, P, P, P, P, P, i32, f32, P, P]),
         "zref_allreduce_sum_direct": (None, [P, i32, u64, P]),
         "zref_allreduce_rs_ag": (None, [P, i32, u64, i32, P, P]),
+        "zref_allreduce_f32_direct": (None, [P, i32, u64, i32, P]),
+        "zref_allreduce_f32_rs_ag": (None, [P, i32, u64, i32, P, P]),
         "zref_zero_bytes_per_rank": (f64, [i32, f64, i32, f64]),
         "zref_ring_send_bytes": (f64, [f64, i32, i32]),
     }
@@ -280,6 +282,24 @@ def allreduce_rs_ag(inputs, average: bool = False):
     outs = [np.empty(n, dtype=np.uint16) for _ in inputs]
     lib().zref_allreduce_rs_ag(_ptr_array(inputs), len(inputs), n, 1 if average else 0,
                                _ptr(scratch), _ptr_array(outs))
+    return outs, scratch
+
+
+def allreduce_f32_direct(inputs, average: bool = False):
+    inputs = [_f32(x) for x in inputs]
+    outs = [np.empty(inputs[0].size, dtype=np.float32) for _ in inputs]
+    lib().zref_allreduce_f32_direct(_ptr_array(inputs), len(inputs), inputs[0].size, 1 if average else 0,
+                                    _ptr_array(outs))
+    return outs
+
+
+def allreduce_f32_rs_ag(inputs, average: bool = False):
+    inputs = [_f32(x) for x in inputs]
+    n = inputs[0].size
+    scratch = np.empty(n, dtype=np.float32)
+    outs = [np.empty(n, dtype=np.float32) for _ in inputs]
+    lib().zref_allreduce_f32_rs_ag(_ptr_array(inputs), len(inputs), n, 1 if average else 0,
+                                   _ptr(scratch), _ptr_array(outs))
     return outs, scratch
 
 

@@ -349,6 +349,49 @@ void zref_allreduce_rs_ag(const uint16_t *const *in, int world, uint64_t n,
     zref_all_gather_bf16(scratch, world, n, out, world);   /* all-gather */
 }
 
+/* fp32 all-reduce, the dtype of the pages' worked example: written
+ * directly (every rank sums all ranks' values in rank order 0..W-1, then
+ * scales by fp32(1/W) when `average`), ... */
+void zref_allreduce_f32_direct(const float *const *in, int world, uint64_t n, int average,
+                               float *const *out)
+{
+    const float scale = (float)(1.0 / (double)world);
+    for (int q = 0; q < world; ++q) {
+        for (uint64_t i = 0; i < n; ++i) {
+            float s = in[0][i];
+            for (int k = 1; k < world; ++k)
+                s = s + in[k][i];
+            out[q][i] = average ? s * scale : s;
+        }
+    }
+}
+
+/* ... and as reduce-scatter into per-rank slices of `scratch` followed by
+ * an all-gather of the slices (the two must agree bit for bit). */
+void zref_allreduce_f32_rs_ag(const float *const *in, int world, uint64_t n, int average,
+                              float *scratch, float *const *out)
+{
+    const float scale = (float)(1.0 / (double)world);
+    for (int r = 0; r < world; ++r) {            /* reduce-scatter */
+        uint64_t lo, hi;
+        shard_range(n, world, r, &lo, &hi);
+        for (uint64_t i = lo; i < hi; ++i) {
+            float s = in[0][i];
+            for (int q = 1; q < world; ++q)
+                s = s + in[q][i];
+            scratch[i] = average ? s * scale : s;
+        }
+    }
+    for (int q = 0; q < world; ++q) {            /* all-gather */
+        for (int r = 0; r < world; ++r) {
+            uint64_t lo, hi;
+            shard_range(n, world, r, &lo, &hi);
+            for (uint64_t i = lo; i < hi; ++i)
+                out[q][i] = scratch[i];
+        }
+    }
+}
+
 /* ------------------------------------------------------- accounting */
 
 /* Per-rank bytes of parameter-related memory (PT "data parallel and ZeRO";

@@ -90,6 +90,42 @@ def pin_worked_example():
         assert np.array_equal(torch_widen(avg[r]), ar / world)
 
 
+def pin_worked_example_fp32():
+    """The same printed example in the page's own dtype (float32 tensors):
+    the fp32 all-reduce, written directly and as reduce-scatter +
+    all-gather, gives [6,10,14,18] on every rank and slice i = element i."""
+    g = golden("collectives_4rank.txt")
+    world = int(g["world"][0][0])
+    x = [np.array(next(r[1:] for r in g["input"] if int(r[0]) == q), dtype=np.float32) for q in range(world)]
+    ar = np.array(g["all_reduce"][0], dtype=np.float32)
+    direct = o.allreduce_f32_direct(x)
+    via, rs = o.allreduce_f32_rs_ag(x)
+    for q in range(world):
+        assert np.array_equal(direct[q], ar) and np.array_equal(via[q], ar)
+    s = o.shard_len(ar.size, world)
+    for rank, val in g["reduce_scatter"]:
+        assert np.array_equal(rs[int(rank) * s:(int(rank) + 1) * s], np.array([float(val)], np.float32))
+    avg = o.allreduce_f32_direct(x, average=True)
+    assert all(np.array_equal(a, ar / world) for a in avg)
+
+
+def pin_allreduce_f32_rank_order():
+    """fp32 all-reduce = numpy's sequential float32 sum over the rank axis
+    (times fp32(1/W) for the mean), ragged n; direct and RS+AG agree."""
+    rng = np.random.default_rng(12)
+    for world in (1, 2, 3, 4, 8, 64):
+        n = 1001
+        x = [(rng.standard_normal(n) * np.exp(rng.uniform(-20, 20))).astype(np.float32) for _ in range(world)]
+        ref = np.cumsum(np.stack(x), axis=0, dtype=np.float32)[-1]
+        for average in (False, True):
+            want = ref * np.float32(1.0 / world) if average else ref
+            direct = o.allreduce_f32_direct(x, average)
+            via, _ = o.allreduce_f32_rs_ag(x, average)
+            for q in range(world):
+                assert np.array_equal(direct[q].view(np.uint32), want.view(np.uint32)), (world, average)
+                assert np.array_equal(via[q].view(np.uint32), want.view(np.uint32)), (world, average)
+
+
 def pin_rs_rank_order():
     """The reduce-scatter sum is an fp32 left fold in rank order (numpy's
     sequential float32 cumsum) scaled by fp32(1/W); ragged n included."""

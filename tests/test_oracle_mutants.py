@@ -41,6 +41,10 @@ MUTANTS = {
     "update_sign_flipped": ("float p = master[i] - s->step_size * u;", "float p = master[i] + s->step_size * u;"),
     "shard_drops_last_element": ("uint64_t a = (uint64_t)r * s, b = a + s;", "uint64_t a = (uint64_t)r * s, b = a + s - 1;"),
     "all_gather_one_replica": ("for (int q = 0; q < n_replicas; ++q) {", "for (int q = 0; q < 1; ++q) {"),
+    "f32_allreduce_drops_last_rank": ("            for (int k = 1; k < world; ++k)\n                s = s + in[k][i];",
+                                      "            for (int k = 1; k < world - 1; ++k)\n                s = s + in[k][i];"),
+    "f32_allreduce_gather_wrong_slice": ("                out[q][i] = scratch[i];", "                out[q][i] = scratch[lo];"),
+    "f32_allreduce_mean_ignored": ("            scratch[i] = average ? s * scale : s;", "            scratch[i] = s;"),
     "stage1_not_sharded": ("case 1: return (2.0 + 2.0) * psi + k * psi / w;", "case 1: return (2.0 + 2.0 + k) * psi;"),
     "ring_missing_factor": ("return op == 0 ? 2.0 * one : one;", "return one;"),
 }
