@@ -313,6 +313,69 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
         torch.distributed.destroy_process_group()
 
 
+def allreduce_arm(args):
+    """The DDP all-reduce path: one zero1_allreduce per step over W emulated
+    ranks' buffers (inputs and outputs distinct).  Reports HBM GB/s of the
+    algorithmic traffic (read W buffers, write W buffers) and, for context
+    with the lecture's figures, the bus bandwidth in the usual convention
+    size * 2(W-1)/W / t."""
+    import zero_sharded_adamw_gb300 as z
+
+    rank, world_size, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    init_dist(world_size, "nccl")
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    w = WL.ALLREDUCE_WORKLOADS[args.ar_workload]
+    code = z.DTYPE_BF16 if w.dtype == torch.bfloat16 else z.DTYPE_F32
+    op = z.OP_AVG if w.average else z.OP_SUM
+    ins = WL.allreduce_inputs(w, dev)
+    outs = [torch.empty_like(ins[0]) for _ in range(w.world)]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        z.zero1_allreduce(w.n, w.world, code, op, ins, outs, err, stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3 if clocks.proc else 0.0)
+    barrier(world_size)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        z.zero1_allreduce(w.n, w.world, code, op, ins, outs, err, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world_size)
+    t1 = time.time()
+    ms = reduce_max(ev0.elapsed_time(ev1), world_size, dev) / args.steps
+    clk = clocks.stop(t0, t1)
+    assert int(err.item()) == 0, "a kernel pipeline wait gave up"
+    size = w.n * ins[0].element_size()
+    hbm_bytes = 2 * w.world * size
+    peak, peak_kind = measured_peak()
+    achieved = hbm_bytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "emulated DDP all-reduce HBM GB/s at 1 GPU", "value": world_size * achieved, "unit": "GB/s",
+        "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_elements": w.n, "emulated_ranks": w.world,
+                   "element": str(w.dtype).replace("torch.", ""), "op": "avg" if w.average else "sum",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "kernel": "zero1_allreduce_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": hbm_bytes, "avg_launch_ms": ms, "peak_kind": peak_kind},
+        "busbw_gbs": size * 2 * (w.world - 1) / w.world / (ms / 1e3) / 1e9,
+        "algbw_gbs": size / (ms / 1e3) / 1e9,
+        "clocks": clk, "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world_size > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -320,6 +383,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="step", choices=["step", "allreduce"],
+                    help="step: the ZeRO-1 optimizer step (default); allreduce: the DDP all-reduce")
+    ap.add_argument("--ar-workload", default="lecture_fp32_w4", choices=sorted(WL.ALLREDUCE_WORKLOADS))
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -335,7 +401,9 @@ def main(argv=None):
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
                  else "working set fits in L2 (launch-latency bound)"}
-    if args.impl == "reference":
+    if args.path == "allreduce" and args.impl == "ours":
+        allreduce_arm(args)
+    elif args.impl == "reference":
         reference_arm(args, w, cfg)
     else:
         ours_arm(args, w, cfg)

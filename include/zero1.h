@@ -217,6 +217,33 @@ int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp, uint64_t 
                        const void *const *grad_ptrs, void *const *param_ptrs,
                        float *master, float *m, float *v, void *stream);
 
+/* Element types and reductions of zero1_allreduce. */
+#define ZERO1_DTYPE_BF16 0
+#define ZERO1_DTYPE_F32  1
+#define ZERO1_OP_SUM     0
+#define ZERO1_OP_AVG     1
+
+/* The data-parallel (DDP) all-reduce of W emulated ranks' buffers
+ * ("Parallel training", "How cards talk: collective communication": every
+ * rank receives the element-wise sum; "Stanford CS336 Lecture 8 close
+ * reading: Parallelism (part 2)", section 7: DDP averages gradients with
+ * all_reduce(op=AVG)).  out_ptrs[q][i] = (in_ptrs[0][i] + in_ptrs[1][i] +
+ * ... + in_ptrs[W-1][i]), summed in fp32 in rank order 0..W-1, times fp32(1/W)
+ * for ZERO1_OP_AVG, rounded to the element type (bf16: nearest even).  Equal
+ * bit for bit to a reduce-scatter followed by an all-gather.
+ *   n: elements per rank (>= 1); world: 1..ZERO1_MAX_WORLD;
+ *   dtype: ZERO1_DTYPE_BF16 or ZERO1_DTYPE_F32; op: ZERO1_OP_SUM or _AVG;
+ *   in_ptrs, out_ptrs: host arrays of W device pointers, 16-byte aligned;
+ *     out_ptrs[r] may equal in_ptrs[r] (in place); other overlaps are not
+ *     allowed.
+ *   errors: optional device word (NULL = none); bit 0 is set if a kernel
+ *     pipeline wait gave up (1 s limit), in which case the outputs are not
+ *     valid.
+ * Asynchronous on `stream`; allocates nothing.  One kernel launch.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_allreduce(uint64_t n, int world, int dtype, int op, const void *const *in_ptrs,
+                    void *const *out_ptrs, unsigned *errors, void *stream);
+
 /* Message for the last error on this thread ("" if none). */
 const char *zero1_last_error(void);
 

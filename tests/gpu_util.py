@@ -26,7 +26,7 @@ class Guarded:
         return self.full.view(torch.int16 if self.dtype == torch.bfloat16 else torch.int32)
 
     def _canary(self):
-        return BF16_CANARY if self.dtype == torch.bfloat16 else F32_CANARY - (1 << 32)
+        return BF16_CANARY if self.dtype == torch.bfloat16 else F32_CANARY
 
     def intact(self) -> bool:
         b = self._bits()

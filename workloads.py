@@ -100,6 +100,39 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class AllReduceWorkload:
+    """An all-reduce of W emulated ranks' buffers of n elements each."""
+    name: str
+    n: int
+    world: int
+    dtype: torch.dtype
+    average: bool
+
+
+# The lecture's benchmark (1e8 fp32 elements, world size 4, sum) and the DDP
+# gradient all-reduce of the GPT-2-small list (bf16, W = 8, mean).
+ALLREDUCE_WORKLOADS = {
+    w.name: w for w in [
+        AllReduceWorkload("lecture_fp32_w4", 100_000_000, 4, torch.float32, False),
+        AllReduceWorkload("ddp_gpt2_small_bf16_w8", GPT2_SMALL_N, 8, torch.bfloat16, True),
+    ]
+}
+
+
+def allreduce_inputs(w: AllReduceWorkload, device) -> list[torch.Tensor]:
+    """Rank r's buffer ~ N(0, 1) from seed 5000 + r, cast to the element type."""
+    out = []
+    for r in range(w.world):
+        g = _gen(5000 + r, device)
+        t = torch.empty(w.n, dtype=w.dtype, device=device)
+        for lo in range(0, w.n, CHUNK):
+            hi = min(lo + CHUNK, w.n)
+            t[lo:hi].copy_(torch.randn(hi - lo, generator=g, device=device))
+        out.append(t)
+    return out
+
+
 def _gen(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)

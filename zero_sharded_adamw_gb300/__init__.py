@@ -22,7 +22,7 @@ __all__ = [
     "zero1_create", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_last_error",
+    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -51,6 +51,7 @@ _SIGS = {
     "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
+    "zero1_allreduce": (_I32, [_U64, _I32, _I32, _I32, _P, _P, _P, _P]),
     "zero1_last_error": (C.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -227,6 +228,16 @@ def zero1_step_noalloc(n: int, world: int, hp: Hparams, t: int, grad_ptrs, param
     c = hp._c()
     _check(_load().zero1_step_noalloc(n, world, C.byref(c), t, _ptrs(grad_ptrs), _ptrs(param_ptrs),
                                       _addr(master), _addr(m), _addr(v), _stream(stream)))
+
+
+DTYPE_BF16, DTYPE_F32 = 0, 1
+OP_SUM, OP_AVG = 0, 1
+
+
+def zero1_allreduce(n: int, world: int, dtype: int, op: int, in_ptrs, out_ptrs, errors=None, stream=None) -> None:
+    """DDP all-reduce of W device buffers (bf16 or fp32, sum or mean)."""
+    _check(_load().zero1_allreduce(n, world, dtype, op, _ptrs(in_ptrs), _ptrs(out_ptrs), _addr(errors),
+                                   _stream(stream)))
 
 
 class Zero1:

@@ -39,9 +39,12 @@
 #include <cuda_runtime.h>
 
 #include "zero1_internal.h"
+#include "zero1_ptx.cuh"
 
 namespace zero1 {
 namespace {
+
+using namespace ptx;
 
 constexpr int kTile = 2048;                      // parameters per tile
 constexpr int kStages = 4;                       // shared-memory ring depth
@@ -50,187 +53,9 @@ constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTi
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kRsThreads = kConsumers + 32;      // + producer warp
 constexpr int kUpdThreads = kConsumers + 64;     // + producer warp + store warp
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 static_assert(kConsumers * kVec == kTile, "one 8-parameter vector per consumer thread");
 
-// ------------------------------------------------------ PTX: TMA, mbarrier
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// True once the phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Global -> shared bulk copy; `bytes` (multiple of 16) are counted on `bar`.
-__device__ __forceinline__ void tma_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(smem_dst)),
-                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void tma_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void tma_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// L2 eviction-priority policies for the cache-hinted copies below.
-__device__ __forceinline__ uint64_t policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tma_load_hint(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
-                                              uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(smem_u32(smem_dst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-// Shared -> global bulk copy in this thread's current bulk group.
-__device__ __forceinline__ void tma_store_hint(void *gdst, const void *smem_src, uint32_t bytes, uint64_t policy)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
-                 "r"(smem_u32(smem_src)), "r"(bytes), "l"(policy)
-                 : "memory");
-}
-
-// 16-byte global store with an L2 eviction-priority hint.
-__device__ __forceinline__ void st_hint(float *dst, float4 v, uint64_t policy)
-{
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
-                 "f"(v.z), "f"(v.w), "l"(policy)
-                 : "memory");
-}
-
-// Drop one 128-byte L2 line without writing it back (dead scratch only).
-__device__ __forceinline__ void discard_l2_line(const void *p)
-{
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
-// Order this thread's generic-proxy shared-memory writes before later
-// async-proxy (bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-// Bounded wait on an mbarrier phase.  Gives up when another thread of the
-// CTA has raised `abort`, or after kWaitLimitNs, raising `abort` and the
-// sticky error bit.  Returns whether the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, DevStatus *status)
-{
-    if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                atomicOr(&status->errors, kErrWaitTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// After an abort, let the producer's last loads land before it exits (the
-// CTA's shared memory must outlive them).  Item k used stage k % kStages,
-// phase (k / kStages) & 1.
-__device__ __forceinline__ void drain_loads(uint64_t *full, uint32_t issued)
-{
-    for (uint32_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k) {
-        const unsigned long long t0 = global_ns();
-        while (!mbar_test(&full[k % kStages], (k / kStages) & 1u) && global_ns() - t0 < kWaitLimitNs) {
-        }
-    }
-}
-
-// ------------------------------------------------------------ bf16 pack
-
-// bf16 -> fp32 widening is exact: the bf16 bits are the top half.
-__device__ __forceinline__ void add_widened(float s[8], uint4 raw)
-{
-    const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        s[2 * k] = __fadd_rn(s[2 * k], __uint_as_float(w[k] << 16));
-        s[2 * k + 1] = __fadd_rn(s[2 * k + 1], __uint_as_float(w[k] & 0xFFFF0000u));
-    }
-}
-
-__device__ __forceinline__ void set_widened(float s[8], uint4 raw)
-{
-    const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        s[2 * k] = __uint_as_float(w[k] << 16);
-        s[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-}
-
-__device__ __forceinline__ unsigned pack2(float lo, float hi)
-{
-    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // .x (lo) -> low 16 bits
-    return *reinterpret_cast<unsigned *>(&b);
-}
 
 // --------------------------------------------------------- kernel params
 
@@ -382,7 +207,7 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
             for (uint32_t b = 0; b * sub < tcta && !*abort; ++b) {
                 for (int grp = 0; grp < ngroups; ++grp, ++k) {
                     const int s = k % kStages;
-                    if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, p.status))
+                    if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, &p.status->errors))
                         break;
                     const int r0 = grp * kRankGroup;
                     const int rn = nw - r0 < kRankGroup ? nw - r0 : kRankGroup;
@@ -402,7 +227,7 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
                     }
                 }
             }
-            if (*abort) drain_loads(sm.full, k);
+            if (*abort) drain_loads<kStages>(sm.full, k);
         }
         return;
     }
@@ -418,7 +243,7 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
         bool ok = true;
         for (int grp = 0; grp < ngroups; ++grp, ++k) {
             const int st = k % kStages;
-            const bool got = mbar_wait(&sm.full[st], (k / kStages) & 1u, abort, p.status);
+            const bool got = mbar_wait(&sm.full[st], (k / kStages) & 1u, abort, &p.status->errors);
             if (!__all_sync(0xFFFFFFFFu, got)) {      // warp-uniform: no lane left behind
                 ok = false;
                 break;
@@ -604,7 +429,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             uint32_t k = 0;
             for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
                 const int s = k % kStages;
-                if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, p.status)) break;
+                if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
                 const uint64_t base = (uint64_t)j * kTile;
                 const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
                 const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
@@ -620,7 +445,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
                 tma_load_hint(sm.in[s][2], p.m + base, cnt * 4u, &sm.full[s], once);
                 tma_load_hint(sm.in[s][3], p.v + base, cnt * 4u, &sm.full[s], once);
             }
-            if (*abort) drain_loads(sm.full, k);
+            if (*abort) drain_loads<kStages>(sm.full, k);
         }
         return;
     }
@@ -629,7 +454,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         uint32_t k = 0;
         for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
             const int s = k % kStages;
-            const bool got = mbar_wait(&sm.done[s], (k / kStages) & 1u, abort, p.status);
+            const bool got = mbar_wait(&sm.done[s], (k / kStages) & 1u, abort, &p.status->errors);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             const uint64_t base = (uint64_t)j * kTile;
             const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
@@ -662,7 +487,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
         const int s = k % kStages;
-        const bool got = mbar_wait(&sm.full[s], (k / kStages) & 1u, abort, p.status);
+        const bool got = mbar_wait(&sm.full[s], (k / kStages) & 1u, abort, &p.status->errors);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint64_t base = (uint64_t)j * kTile;
         const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
