@@ -70,6 +70,9 @@ def _signatures():
         "zref_step": (None, [u64, i32, P, u64, P, P, P, P, P, P, i32, f32, P, P]),
         "zref_allreduce_sum_direct": (None, [P, i32, u64, P]),
         "zref_allreduce_rs_ag": (None, [P, i32, u64, i32, P, P]),
+        "zref_clip_coef_ex": (f32, [f64, f64, f64]),
+        "zref_adamw_range_ex": (None, [P, P, P, P, u64, f32, P, P]),
+        "zref_step_ex": (None, [u64, i32, P, P, u64, P, P, P, P, P, P, i32, f32, P, P]),
         "zref_allreduce_f32_direct": (None, [P, i32, u64, i32, P]),
         "zref_allreduce_f32_rs_ag": (None, [P, i32, u64, i32, P, P]),
         "zref_zero_bytes_per_rank": (f64, [i32, f64, i32, f64]),
@@ -265,6 +268,62 @@ def step(state: State, grads, hp: HP, clip_override: float | None = None):
                     1 if clip_override is not None else 0,
                     C.c_float(0.0 if clip_override is None else clip_override),
                     C.byref(norm), C.byref(clip))
+    return reps, float(norm.value), np.float32(clip.value)
+
+
+class _COptions(C.Structure):
+    _fields_ = [("decay_before_update", C.c_int), ("clip_eps", C.c_double), ("moments_bf16", C.c_int)]
+
+
+@dataclass
+class Options:
+    """Step variants: torch's decay-first order, clip eps, bf16 moments."""
+    decay_before_update: bool = False
+    clip_eps: float = 0.0
+    moments_bf16: bool = False
+
+    def c(self) -> _COptions:
+        return _COptions(1 if self.decay_before_update else 0, self.clip_eps, 1 if self.moments_bf16 else 0)
+
+
+def state_ex(master, options: Options) -> State:
+    """A fresh state (m = v = 0) whose moments have the options' storage type."""
+    st = State(master)
+    if options.moments_bf16:
+        st.m = np.zeros(st.master.size, np.uint16)
+        st.v = np.zeros(st.master.size, np.uint16)
+    return st
+
+
+def clip_coef_ex(norm: float, max_norm: float, clip_eps: float) -> np.float32:
+    return np.float32(lib().zref_clip_coef_ex(norm, max_norm, clip_eps))
+
+
+def adamw_range_ex(master, m, v, ghat, c: float, scalars: dict, options: Options) -> None:
+    s = Scalars(*[scalars[k] for k, _ in Scalars._fields_])
+    o = options.c()
+    for a in (master, m, v, ghat):
+        assert a.flags["C_CONTIGUOUS"]
+    lib().zref_adamw_range_ex(_ptr(master), _ptr(m), _ptr(v), _ptr(ghat), master.size, C.c_float(c),
+                              C.byref(s), C.byref(o))
+
+
+def step_ex(state: State, grads, hp: HP, options: Options, clip_override: float | None = None):
+    """One step with options; state.m/state.v are uint16 when moments_bf16."""
+    grads = [_u16(g) for g in grads]
+    world, n = len(grads), grads[0].size
+    want = np.uint16 if options.moments_bf16 else np.float32
+    assert state.m.dtype == want and state.v.dtype == want
+    state.t += 1
+    reps = [np.empty(n, dtype=np.uint16) for _ in range(world)]
+    ghat = np.empty(n, dtype=np.float32)
+    norm, clip = C.c_double(), C.c_float()
+    h, o = hp.c(), options.c()
+    lib().zref_step_ex(n, world, C.byref(h), C.byref(o), state.t, _ptr_array(grads), _ptr_array(reps),
+                       _ptr(state.master), _ptr(state.m), _ptr(state.v), _ptr(ghat),
+                       1 if clip_override is not None else 0,
+                       C.c_float(0.0 if clip_override is None else clip_override),
+                       C.byref(norm), C.byref(clip))
     return reps, float(norm.value), np.float32(clip.value)
 
 

@@ -42,6 +42,11 @@
  * Parity pins: every function below is pinned by the not-gpu tests against
  * the pages' printed values, closed forms, torch.optim.AdamW special cases,
  * numpy/torch library routines and brute force (see tests/test_oracle_*.py).
+ * One exception, "parity unpinned": the intermediate bf16 roundings of the
+ * bf16-moment variant (zref_adamw_range_ex with moments_bf16).  The pages
+ * only say that some configurations store m and v in bf16; the per-op
+ * rounding sequence is a reading, tied to the fp32-moment oracle by bounds
+ * and to closed forms only within bf16 precision.
  */
 #include <stdint.h>
 #include <string.h>
@@ -248,6 +253,79 @@ void zref_adamw_range(float *master, float *m, float *v, const float *ghat,
     }
 }
 
+/* ------------------------------------------------------ step variants */
+
+/* Variants the pages name beside the default step:
+ *   decay_before_update -- torch.optim.AdamW's order, p = p*(1-lr*wd) then
+ *       p = p - step_size*(m/d) ("Parallel training", "mixed precision and
+ *       AdamW": PyTorch decays first, the page's code decays after);
+ *   clip_eps -- c = min(1, max_norm/(norm + clip_eps)), the form
+ *       torch.nn.utils.clip_grad_norm_ uses with 1e-6; 0 is the page's rule;
+ *   moments_bf16 -- m and v stored in bf16 ("some configurations store m, v
+ *       in bf16, 12 bytes per parameter in total"): each in-place op on a
+ *       moment computes in fp32 and rounds its result to bf16, so
+ *       m = bf16(bf16(b1*m) + (1-b1)*g), v likewise, d = bf16(bf16(sqrt(v))
+ *       + eps); the fp32 master update reads those bf16 values. */
+typedef struct {
+    int decay_before_update;
+    double clip_eps;
+    int moments_bf16;
+} zref_options;
+
+float zref_clip_coef_ex(double norm, double max_norm, double clip_eps)
+{
+    if (!(max_norm > 0.0))
+        return 1.0f;
+    if (isnan(norm))
+        return (float)NAN;
+    double q = max_norm / (norm + clip_eps);
+    return q < 1.0 ? (float)q : 1.0f;
+}
+
+static float bf16_round(float x) { return zref_bf16_to_f32(zref_f32_to_bf16(x)); }
+
+/* AdamW on one slice with options.  m and v point at float arrays, or at
+ * uint16_t bf16 arrays when moments_bf16. */
+void zref_adamw_range_ex(float *master, void *m, void *v, const float *ghat, uint64_t count, float c,
+                         const zref_scalars *s, const zref_options *o)
+{
+    for (uint64_t i = 0; i < count; ++i) {
+        float g = ghat[i] * c;
+        float mi, vi, d;
+        if (o->moments_bf16) {
+            uint16_t *mb = (uint16_t *)m, *vb = (uint16_t *)v;
+            mi = bf16_round(s->beta1 * zref_bf16_to_f32(mb[i]));
+            mi = bf16_round(mi + s->one_minus_beta1 * g);
+            vi = bf16_round(s->beta2 * zref_bf16_to_f32(vb[i]));
+            float og = s->one_minus_beta2 * g;
+            vi = bf16_round(vi + og * g);
+            d = bf16_round(bf16_round(sqrtf(vi)) + s->eps);
+            mb[i] = zref_f32_to_bf16(mi);
+            vb[i] = zref_f32_to_bf16(vi);
+        } else {
+            float *mf = (float *)m, *vf = (float *)v;
+            mi = s->beta1 * mf[i];
+            mi = mi + s->one_minus_beta1 * g;
+            vi = s->beta2 * vf[i];
+            float og = s->one_minus_beta2 * g;
+            vi = vi + og * g;
+            d = sqrtf(vi) + s->eps;
+            mf[i] = mi;
+            vf[i] = vi;
+        }
+        float u = mi / d;
+        float p = master[i];
+        if (o->decay_before_update) {
+            p = p * s->decay;
+            p = p - s->step_size * u;
+        } else {
+            p = p - s->step_size * u;
+            p = p * s->decay;
+        }
+        master[i] = p;
+    }
+}
+
 /* --------------------------------------------------------- all-gather */
 
 /* bf16 cast of the fp32 master (PT: "cast a bf16 copy for the forward each
@@ -298,6 +376,38 @@ void zref_step(uint64_t n, int world, const zref_hparams *hp, uint64_t t,
         uint64_t lo, hi;
         shard_range(n, world, r, &lo, &hi);
         zref_adamw_range(master + lo, m + lo, v + lo, ghat + lo, hi - lo, c, &s);
+    }
+
+    zref_all_gather_bf16(master, world, n, replicas, world);
+
+    if (norm_out) *norm_out = norm;
+    if (clip_out) *clip_out = c;
+}
+
+/* One step with options; m and v as in zref_adamw_range_ex. */
+void zref_step_ex(uint64_t n, int world, const zref_hparams *hp, const zref_options *o, uint64_t t,
+                  const uint16_t *const *grads, uint16_t *const *replicas,
+                  float *master, void *m, void *v, float *ghat,
+                  int use_override, float clip_override,
+                  double *norm_out, float *clip_out)
+{
+    zref_scalars s;
+    zref_step_scalars(hp, world, t, &s);
+
+    zref_reduce_scatter_mean(grads, world, n, ghat);
+
+    zref_norm_acc acc;
+    zref_norm_acc_init(&acc);
+    zref_norm_acc_add(&acc, ghat, n);
+    double norm = zref_norm_acc_value(&acc);
+    float c = use_override ? clip_override : zref_clip_coef_ex(norm, hp->max_norm, o->clip_eps);
+
+    const size_t msz = o->moments_bf16 ? sizeof(uint16_t) : sizeof(float);
+    for (int r = 0; r < world; ++r) {
+        uint64_t lo, hi;
+        shard_range(n, world, r, &lo, &hi);
+        zref_adamw_range_ex(master + lo, (char *)m + lo * msz, (char *)v + lo * msz, ghat + lo, hi - lo, c,
+                            &s, o);
     }
 
     zref_all_gather_bf16(master, world, n, replicas, world);

@@ -395,6 +395,115 @@ def pin_full_step_brute_force():
         assert bf16_ulp_distance(reps[0], ref_b).max() <= 1
 
 
+def pin_step_ex_default_is_step():
+    """The options entry with every option off is the default step, bit for bit."""
+    rng = np.random.default_rng(30)
+    n, world = 1001, 4
+    hp = o.HP(max_norm=0.05)
+    a, b = o.State((rng.standard_normal(n) * 0.02).astype(np.float32)), None
+    b = a.copy()
+    for _ in range(3):
+        grads = [rand_bf16(rng, n, 0.01) for _ in range(world)]
+        ra, na, ca = o.step(a, grads, hp)
+        rb, nb, cb = o.step_ex(b, grads, hp, o.Options())
+        assert na == nb and ca == cb
+        assert all(np.array_equal(x, y) for x, y in zip(ra, rb))
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def pin_decay_first_vs_torch_adamw():
+    """decay_before_update is torch.optim.AdamW's own order: ten steps equal
+    float64 torch.optim.AdamW with weight decay on (eps scaled as before)."""
+    rng = np.random.default_rng(31)
+    n, world = 16, 4
+    hp = o.HP(lr=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.5, max_norm=0.0)
+    p0 = rng.uniform(0.5, 1.0, n).astype(np.float32)
+    st = o.state_ex(p0, o.Options(decay_before_update=True))
+    p = torch.nn.Parameter(torch.tensor(p0, dtype=torch.float64))
+    opt = torch.optim.AdamW([p], lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps,
+                            weight_decay=hp.weight_decay, foreach=False)
+    for t in range(1, 11):
+        grads = [rand_bf16(rng, n, 1e-2) for _ in range(world)]
+        o.step_ex(st, grads, hp, o.Options(decay_before_update=True))
+        p.grad = torch.tensor(np.mean([torch_widen(g).astype(np.float64) for g in grads], axis=0))
+        opt.param_groups[0]["eps"] = hp.eps / math.sqrt(1.0 - hp.beta2 ** t)
+        opt.step()
+    ref = p.detach().numpy()
+    assert np.allclose(st.master, ref, rtol=2e-6, atol=0)
+    # the page's order differs visibly at this lr * wd
+    st2 = o.state_ex(p0, o.Options())
+    rng = np.random.default_rng(31)
+    for t in range(1, 11):
+        o.step_ex(st2, [rand_bf16(rng, n, 1e-2) for _ in range(world)], hp, o.Options())
+    assert np.abs(st2.master - ref).max() > 1e3 * 2e-6 * np.abs(ref).max()
+
+
+def pin_clip_eps_vs_torch_clip_grad_norm():
+    """clip_eps = 1e-6 is torch.nn.utils.clip_grad_norm_'s coefficient
+    min(1, max_norm/(norm + 1e-6)); with decay first the whole step equals
+    clip_grad_norm_ followed by torch.optim.AdamW (float64)."""
+    for norm, mx in ((3.0, 1.0), (0.5, 1.0), (1.0, 1.0), (1.0 + 5e-7, 1.0), (1e-3, 1e-3)):
+        g = torch.tensor([norm], dtype=torch.float64, requires_grad=True)
+        g.grad = torch.tensor([norm], dtype=torch.float64)
+        torch.nn.utils.clip_grad_norm_([g], mx)
+        want = float(g.grad[0]) / norm
+        assert abs(float(o.clip_coef_ex(norm, mx, 1e-6)) - want) <= 1e-7 * want, (norm, mx)
+    rng = np.random.default_rng(32)
+    n, world = 13, 4
+    hp = o.HP(lr=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.05)
+    opts = o.Options(decay_before_update=True, clip_eps=1e-6)
+    p0 = (rng.standard_normal(n) * 0.5).astype(np.float32)
+    st = o.state_ex(p0, opts)
+    p = torch.nn.Parameter(torch.tensor(p0, dtype=torch.float64))
+    opt = torch.optim.AdamW([p], lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps,
+                            weight_decay=hp.weight_decay, foreach=False)
+    for t in range(1, 6):
+        grads = [rand_bf16(rng, n, 0.1) for _ in range(world)]
+        _, _, c = o.step_ex(st, grads, hp, opts)
+        p.grad = torch.tensor(np.mean([torch_widen(x).astype(np.float64) for x in grads], axis=0))
+        torch.nn.utils.clip_grad_norm_([p], hp.max_norm)
+        opt.param_groups[0]["eps"] = hp.eps / math.sqrt(1.0 - hp.beta2 ** t)
+        opt.step()
+        assert c < 1.0
+    assert np.allclose(st.master, p.detach().numpy(), rtol=1e-5, atol=1e-6 * np.abs(p0).max())
+
+
+def pin_bf16_moments_bounds():
+    """bf16 moments: stored values are bf16, v >= 0; over ten steps m and v
+    stay within bf16 rounding of the fp32-moment oracle's (relative 2^-6 of
+    the array scale) and the master within 1e-3 relative; with a constant
+    gradient and eps = 0 every step still moves by lr*sign(g) to within the
+    bf16 precision of m/sqrt(v)."""
+    rng = np.random.default_rng(33)
+    n, world = 4099, 4
+    hp = o.HP(lr=1e-3, max_norm=0.0)
+    p0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    a, b = o.state_ex(p0, o.Options()), o.state_ex(p0, o.Options(moments_bf16=True))
+    for _ in range(10):
+        grads = [rand_bf16(rng, n, 1e-2) for _ in range(world)]
+        o.step_ex(a, grads, hp, o.Options())
+        ra, _, _ = o.step_ex(b, grads, hp, o.Options(moments_bf16=True))
+    bm, bv = o.bf16_to_f32(b.m), o.bf16_to_f32(b.v)
+    assert (bv >= 0).all()
+    for x, ref in ((bm, a.m), (bv, a.v)):
+        scale = np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+        assert np.abs(x - ref).max() <= 2.0 ** -6 * max(scale, 1e-30) + 2.0 ** -7 * np.abs(ref).max()
+    assert np.abs(b.master - a.master).max() <= 1e-3 * np.abs(a.master).max()
+    assert np.array_equal(ra[0], o.f32_to_bf16(b.master))
+    # constant gradient, eps = 0
+    lr = 1e-2
+    hp2 = o.HP(lr=lr, beta1=0.9, beta2=0.95, eps=0.0, weight_decay=0.0, max_norm=0.0)
+    p = rng.uniform(0.5, 1.0, 64).astype(np.float32)
+    g = o.f32_to_bf16(np.where(rng.random(64) < 0.5, -0.25, 0.5).astype(np.float32))
+    st = o.state_ex(p, o.Options(moments_bf16=True))
+    sgn = np.sign(o.bf16_to_f32(g)).astype(np.float64)
+    for _ in range(10):
+        before = st.master.astype(np.float64)
+        o.step_ex(st, [g, g], hp2, o.Options(moments_bf16=True))
+        assert np.abs((before - st.master) - lr * sgn).max() <= lr * 2.0 ** -6
+
+
 def pin_ddp_linearity():
     """The printed DDP check (float64): the mean of the 4 shard gradients is
     the full-batch gradient.  The oracle's reduce-scatter mean of the bf16

@@ -1,7 +1,8 @@
 """Each plausible mistake planted in a copy of the oracle trips at least one pin.
 
 A mutant is the oracle source with one textual substitution (a dropped term,
-a wrong sign or index, a swapped operand, a changed order), compiled with the
+a wrong sign or index, a swapped operand, a changed order) applied at every
+place the text occurs (the same mistake made consistently), compiled with the
 oracle's own flags into a temporary library.  The pins in oracle_pins.py run
 against it; the test fails if all of them still pass.
 """
@@ -45,6 +46,9 @@ MUTANTS = {
                                       "            for (int k = 1; k < world - 1; ++k)\n                s = s + in[k][i];"),
     "f32_allreduce_gather_wrong_slice": ("                out[q][i] = scratch[i];", "                out[q][i] = scratch[lo];"),
     "f32_allreduce_mean_ignored": ("            scratch[i] = average ? s * scale : s;", "            scratch[i] = s;"),
+    "variant_decay_order_ignored": ("        if (o->decay_before_update) {", "        if (0) {"),
+    "variant_clip_eps_ignored": ("    double q = max_norm / (norm + clip_eps);", "    double q = max_norm / norm;"),
+    "variant_bf16_v_not_stored": ("            vb[i] = zref_f32_to_bf16(vi);", "            (void)vb;"),
     "stage1_not_sharded": ("case 1: return (2.0 + 2.0) * psi + k * psi / w;", "case 1: return (2.0 + 2.0 + k) * psi;"),
     "ring_missing_factor": ("return op == 0 ? 2.0 * one : one;", "return one;"),
 }
@@ -59,7 +63,7 @@ def source():
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, source, tmp_path):
     old, new = MUTANTS[name]
-    assert source.count(old) == 1, f"mutation site for {name} not found exactly once"
+    assert source.count(old) >= 1, f"mutation site for {name} not found"
     src = tmp_path / "mutant.c"
     src.write_text(source.replace(old, new))
     so = tmp_path / "libmutant.so"
