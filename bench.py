@@ -215,9 +215,10 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     stream = torch.cuda.current_stream(dev)
 
     hp = z.Hparams(**w.hparams())
+    opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16)
     grad_sets = [WL.grads(w, t, dev) for t in (1, 2)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
-    opt = z.Zero1(w.n, w.world, hp)
+    opt = z.Zero1(w.n, w.world, hp, opts)
     opt.set_state(WL.master(w, dev), stream=stream)
     torch.cuda.synchronize(dev)
 
@@ -247,11 +248,12 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
 
     ms_per_step = ms / args.steps
     value = world_size * w.n * args.steps / (ms / 1e3)
-    alg_step = w.bytes_per_step()
+    state_rw = 16 if args.moments_bf16 else 24          # master, m, v read + write
+    alg_step = (4 * w.world + state_rw) * w.n
     peak, peak_kind = measured_peak()
     upd_avg = upd_ms / max(1, prof_steps)
     rs_avg = rs_ms / max(1, prof_steps)
-    upd_bytes = (24 + 2 * w.world) * w.n          # state read+write, replica writes
+    upd_bytes = (state_rw + 2 * w.world) * w.n    # state read+write, replica writes
     rs_bytes = (2 * w.world) * w.n                # gradient reads
     traffic = kernel_traffic(w.name)
     achieved = upd_bytes / (upd_avg / 1e3) / 1e9
@@ -389,6 +391,9 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--moments-bf16", action="store_true", help="variant: m and v stored in bf16")
+    ap.add_argument("--decay-first", action="store_true", help="variant: torch.optim.AdamW's decay order")
+    ap.add_argument("--clip-eps", type=float, default=0.0, help="variant: clip eps (torch uses 1e-6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -397,7 +402,9 @@ def main(argv=None):
     if args.n is not None:
         w = w.with_n(args.n)
     cfg = {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
-           "bytes_per_param": 4 * w.world + 24, "hparams": w.hparams(),
+           "bytes_per_param": 4 * w.world + (16 if args.moments_bf16 else 24), "hparams": w.hparams(),
+           "variant": {"moments_bf16": args.moments_bf16, "decay_first": args.decay_first,
+                       "clip_eps": args.clip_eps},
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
                  else "working set fits in L2 (launch-latency bound)"}

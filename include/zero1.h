@@ -96,6 +96,32 @@ typedef struct zero1_ctx *zero1_handle;
  * On error *out is set to NULL. */
 int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *out);
 
+/* Variants of the step the pages name beside the default (all zero = the
+ * default step of zero1_create):
+ *   decay_before_update: 1 = torch.optim.AdamW's order, p = p*(1-lr*wd) and
+ *     then p = p - step_size*m/(sqrt(v)+eps); 0 = after the update, as the
+ *     page's code does ("Parallel training", "mixed precision and AdamW").
+ *   clip_eps: c = min(1, max_norm/(norm + clip_eps)); 0 is the page's rule,
+ *     torch.nn.utils.clip_grad_norm_ uses 1e-6.
+ *   moments_bf16: 1 = m and v stored in bf16 (the pages' note that some
+ *     configurations keep them in bf16: 12 bytes per parameter in all); each
+ *     moment update computes in fp32 and rounds to bf16 per operation:
+ *     m = bf16(bf16(b1*m) + (1-b1)*g), v = bf16(bf16(b2*v) + (1-b2)*g*g),
+ *     d = bf16(bf16(sqrt(v)) + eps); the fp32 master update uses those.
+ *   size: sizeof(zero1_options) (lets the struct grow). */
+typedef struct zero1_options {
+    uint32_t size;
+    int32_t decay_before_update;
+    double clip_eps;
+    int32_t moments_bf16;
+} zero1_options;
+
+/* zero1_create with step variants (opts may be NULL: the default step).
+ * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
+ * negative or non-finite clip_eps. */
+int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
+                    zero1_handle *out);
+
 /* Free the handle and its device memory after synchronizing the device.
  * NULL is accepted and ignored.  Returns ZERO1_OK or ZERO1_ECUDA. */
 int zero1_destroy(zero1_handle h);
@@ -128,28 +154,29 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
 
 /* Checkpoint restore ("Parallel training", "training loop and checkpoint":
- * a checkpoint carries m, v and t).  master, m, v: fp32 arrays of n entries
- * in device or host memory (copied with cudaMemcpyDefault); m or v may be
+ * a checkpoint carries m, v and t).  master, m, v: arrays of n entries in
+ * device or host memory (copied with cudaMemcpyDefault): master fp32, m and
+ * v fp32, or bf16 for a handle created with moments_bf16; m or v may be
  * NULL, meaning zeros.  t: the number of steps already taken (the next step
  * uses t+1).  Enqueued on `stream`; a pageable host source is consumed
  * before the call returns.  Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
-int zero1_set_state(zero1_handle h, const float *master, const float *m, const float *v,
+int zero1_set_state(zero1_handle h, const float *master, const void *m, const void *v,
                     uint64_t t, void *stream);
 
 /* Checkpoint save: copies master, m, v (n fp32 each) into device or host
  * arrays (any may be NULL to skip it) and writes the step count to *t (may
  * be NULL).  Enqueued on `stream`; synchronize it before reading a host
  * destination. */
-int zero1_get_state(zero1_handle h, float *master, float *m, float *v, uint64_t *t, void *stream);
+int zero1_get_state(zero1_handle h, float *master, void *m, void *v, uint64_t *t, void *stream);
 
 /* The same two copies for parameters [offset, offset+count) only -- one
  * rank's shard is offset = r*S, count = min(S, n - r*S) -- so that each rank
  * can save or load its own slice.  The step count is untouched.
  * Errors: ZERO1_EINVAL (range outside [0, n), NULL master for set). */
 int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const float *master,
-                          const float *m, const float *v, void *stream);
+                          const void *m, const void *v, void *stream);
 int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float *master,
-                          float *m, float *v, void *stream);
+                          void *m, void *v, void *stream);
 
 /* Change the learning rate used by later steps (schedules such as warmup +
  * cosine, "Parallel training", "training loop and checkpoint").

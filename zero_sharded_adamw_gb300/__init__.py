@@ -18,8 +18,8 @@ import os
 from dataclasses import dataclass
 
 __all__ = [
-    "Zero1Error", "Hparams", "Zero1",
-    "zero1_create", "zero1_destroy", "zero1_step", "zero1_step_host",
+    "Zero1Error", "Hparams", "Options", "Zero1",
+    "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
     "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_last_error",
@@ -36,6 +36,7 @@ ERRORS = {-1: "ZERO1_EINVAL", -2: "ZERO1_EALIGN", -3: "ZERO1_ENOMEM", -4: "ZERO1
 _P, _U64, _I32, _F64 = C.c_void_p, C.c_uint64, C.c_int, C.c_double
 _SIGS = {
     "zero1_create": (_I32, [_U64, _I32, _P, _P]),
+    "zero1_create_ex": (_I32, [_U64, _I32, _P, _P, _P]),
     "zero1_destroy": (_I32, [_P]),
     "zero1_step": (_I32, [_P, _P, _P, _P]),
     "zero1_step_host": (_I32, [_P, _P, _P, _P]),
@@ -79,6 +80,24 @@ class Hparams:
 
     def _c(self) -> _CHparams:
         return _CHparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.max_norm)
+
+
+class _COptions(C.Structure):
+    _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
+                ("moments_bf16", C.c_int32)]
+
+
+@dataclass
+class Options:
+    """Step variants: torch.optim.AdamW's decay order, a clip eps (torch's
+    clip_grad_norm_ uses 1e-6), m and v stored in bf16."""
+    decay_before_update: bool = False
+    clip_eps: float = 0.0
+    moments_bf16: bool = False
+
+    def _c(self) -> _COptions:
+        return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
+                         1 if self.moments_bf16 else 0)
 
 
 _lib = None
@@ -143,6 +162,15 @@ def zero1_create(n: int, world: int, hp: Hparams | None = None) -> int:
     h = C.c_void_p()
     c = (hp or Hparams())._c()
     _check(_load().zero1_create(n, world, C.byref(c), C.byref(h)))
+    return h.value
+
+
+def zero1_create_ex(n: int, world: int, hp: Hparams | None = None, opts: Options | None = None) -> int:
+    """Create a handle with step variants."""
+    h = C.c_void_p()
+    c = (hp or Hparams())._c()
+    o = (opts or Options())._c()
+    _check(_load().zero1_create_ex(n, world, C.byref(c), C.byref(o), C.byref(h)))
     return h.value
 
 
@@ -243,9 +271,9 @@ def zero1_allreduce(n: int, world: int, dtype: int, op: int, in_ptrs, out_ptrs, 
 class Zero1:
     """Owning wrapper around a handle (closes on ``close()`` / context exit)."""
 
-    def __init__(self, n: int, world: int, hp: Hparams | None = None):
-        self.n, self.world, self.hp = n, world, hp or Hparams()
-        self.handle = zero1_create(n, world, self.hp)
+    def __init__(self, n: int, world: int, hp: Hparams | None = None, opts: Options | None = None):
+        self.n, self.world, self.hp, self.opts = n, world, hp or Hparams(), opts or Options()
+        self.handle = zero1_create_ex(n, world, self.hp, self.opts)
 
     def step(self, grads, params, stream=None) -> None:
         zero1_step(self.handle, grads, params, stream)

@@ -38,7 +38,10 @@ struct zero1_ctx {
     bool reread = false;         // W <= 2: the update kernel re-reads the gradients
     void *block = nullptr;       // one cudaMalloc holding everything below
     uint64_t block_bytes = 0;
-    float *master = nullptr, *m = nullptr, *v = nullptr, *ghat = nullptr;
+    float *master = nullptr, *ghat = nullptr;
+    unsigned char *m = nullptr, *v = nullptr;   // fp32 or bf16 elements (msz bytes each)
+    zero1_options opts{};
+    size_t msz = sizeof(float);
     double *partials = nullptr;
     zero1::DevStatus *status = nullptr;
     // host-path staging (zero1_step_host), allocated on first use, and the
@@ -142,6 +145,11 @@ const char *zero1_last_error(void) { return g_err; }
 
 int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *out)
 {
+    return zero1_create_ex(n, world, hp, nullptr, out);
+}
+
+int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts, zero1_handle *out)
+{
     g_err[0] = '\0';
     if (out == nullptr) return fail(ZERO1_EINVAL, "out is NULL");
     *out = nullptr;
@@ -152,6 +160,13 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
     if (n > (uint64_t)1 << 50) return fail(ZERO1_EINVAL, "n too large");
     int rc = check_hparams(hp);
     if (rc) return rc;
+    zero1_options o{};
+    o.size = sizeof(zero1_options);
+    if (opts) {
+        if (opts->size != sizeof(zero1_options)) return fail(ZERO1_EINVAL, "opts->size must be sizeof(zero1_options)");
+        if (!finite_nonneg(opts->clip_eps)) return fail(ZERO1_EINVAL, "clip_eps must be finite and >= 0");
+        o = *opts;
+    }
 
     int dev = 0, count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -170,6 +185,8 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
     h->hp = *hp;
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
+    h->opts = o;
+    h->msz = o.moments_bf16 ? 2 : sizeof(float);
     zero1_shard_plan(n, world, &h->shard, &h->padded);
     h->reread = world <= 2;
     zero1::plan_grids(world, n, h->reread, h->num_sms, &h->grid_rs, &h->grid_update);
@@ -177,21 +194,23 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
     // One allocation: master | m | v | ghat (W >= 3) | partials | status,
     // every section 256-byte aligned.
     const uint64_t state_bytes = round_up(h->padded * sizeof(float), 256);
+    const uint64_t mom_bytes = round_up(h->padded * h->msz, 256);
     const uint64_t ghat_bytes = h->reread ? 0 : state_bytes;
     const uint64_t part_bytes = round_up(2 * (uint64_t)h->grid_rs * sizeof(double), 256);
     const uint64_t status_bytes = 256;
-    h->block_bytes = 3 * state_bytes + ghat_bytes + part_bytes + status_bytes;
+    const uint64_t st3 = state_bytes + 2 * mom_bytes;
+    h->block_bytes = st3 + ghat_bytes + part_bytes + status_bytes;
     if ((e = cudaMalloc(&h->block, h->block_bytes)) != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc of optimizer state");
     }
     char *base = static_cast<char *>(h->block);
     h->master = reinterpret_cast<float *>(base);
-    h->m = reinterpret_cast<float *>(base + state_bytes);
-    h->v = reinterpret_cast<float *>(base + 2 * state_bytes);
-    h->ghat = h->reread ? nullptr : reinterpret_cast<float *>(base + 3 * state_bytes);
-    h->partials = reinterpret_cast<double *>(base + 3 * state_bytes + ghat_bytes);
-    h->status = reinterpret_cast<zero1::DevStatus *>(base + 3 * state_bytes + ghat_bytes + part_bytes);
+    h->m = reinterpret_cast<unsigned char *>(base + state_bytes);
+    h->v = reinterpret_cast<unsigned char *>(base + state_bytes + mom_bytes);
+    h->ghat = h->reread ? nullptr : reinterpret_cast<float *>(base + st3);
+    h->partials = reinterpret_cast<double *>(base + st3 + ghat_bytes);
+    h->status = reinterpret_cast<zero1::DevStatus *>(base + st3 + ghat_bytes + part_bytes);
     if ((e = cudaMemset(h->block, 0, h->block_bytes)) != cudaSuccess ||
         (e = cudaDeviceSynchronize()) != cudaSuccess) {
         cudaFree(h->block);
@@ -257,6 +276,9 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.max_norm = h->hp.max_norm;
     s.grid_rs = h->grid_rs;
     s.grid_update = h->grid_update;
+    s.moments_bf16 = h->opts.moments_bf16 != 0;
+    s.decay_first = h->opts.decay_before_update != 0;
+    s.clip_eps = h->opts.clip_eps;
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
@@ -350,7 +372,7 @@ int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *
 }
 
 int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const float *master,
-                          const float *m, const float *v, void *stream)
+                          const void *m, const void *v, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (!master) return fail(ZERO1_EINVAL, "master is NULL");
@@ -362,17 +384,18 @@ int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const
     cudaError_t e;
     if ((e = cudaMemcpyAsync(h->master + offset, master, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
         return cuda_fail(e, "master copy");
-    e = m ? cudaMemcpyAsync(h->m + offset, m, bytes, cudaMemcpyDefault, st)
-          : cudaMemsetAsync(h->m + offset, 0, bytes, st);
+    const uint64_t mbytes = count * h->msz;
+    e = m ? cudaMemcpyAsync(h->m + offset * h->msz, m, mbytes, cudaMemcpyDefault, st)
+          : cudaMemsetAsync(h->m + offset * h->msz, 0, mbytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "m copy");
-    e = v ? cudaMemcpyAsync(h->v + offset, v, bytes, cudaMemcpyDefault, st)
-          : cudaMemsetAsync(h->v + offset, 0, bytes, st);
+    e = v ? cudaMemcpyAsync(h->v + offset * h->msz, v, mbytes, cudaMemcpyDefault, st)
+          : cudaMemsetAsync(h->v + offset * h->msz, 0, mbytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "v copy");
     return ZERO1_OK;
 }
 
 int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float *master,
-                          float *m, float *v, void *stream)
+                          void *m, void *v, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (offset > h->n || count > h->n - offset) return fail(ZERO1_EINVAL, "range outside [0, n)");
@@ -383,14 +406,15 @@ int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float
     cudaError_t e;
     if (master && (e = cudaMemcpyAsync(master, h->master + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
         return cuda_fail(e, "master copy");
-    if (m && (e = cudaMemcpyAsync(m, h->m + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+    const uint64_t mbytes = count * h->msz;
+    if (m && (e = cudaMemcpyAsync(m, h->m + offset * h->msz, mbytes, cudaMemcpyDefault, st)) != cudaSuccess)
         return cuda_fail(e, "m copy");
-    if (v && (e = cudaMemcpyAsync(v, h->v + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
+    if (v && (e = cudaMemcpyAsync(v, h->v + offset * h->msz, mbytes, cudaMemcpyDefault, st)) != cudaSuccess)
         return cuda_fail(e, "v copy");
     return ZERO1_OK;
 }
 
-int zero1_set_state(zero1_handle h, const float *master, const float *m, const float *v, uint64_t t, void *stream)
+int zero1_set_state(zero1_handle h, const float *master, const void *m, const void *v, uint64_t t, void *stream)
 {
     int rc = zero1_set_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
     if (rc) return rc;
@@ -398,7 +422,7 @@ int zero1_set_state(zero1_handle h, const float *master, const float *m, const f
     return ZERO1_OK;
 }
 
-int zero1_get_state(zero1_handle h, float *master, float *m, float *v, uint64_t *t, void *stream)
+int zero1_get_state(zero1_handle h, float *master, void *m, void *v, uint64_t *t, void *stream)
 {
     int rc = zero1_get_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
     if (rc) return rc;

@@ -39,7 +39,8 @@ struct StepLaunch {
     void *const *params;        // W device pointers (bf16, n entries)
     int world;
     uint64_t n;
-    float *master, *m, *v;      // fp32 state, n (padded) entries, 256-B aligned
+    float *master;              // fp32 master, n (padded) entries, 256-B aligned
+    void *m, *v;                // fp32 moments, or bf16 when moments_bf16
     float *ghat;                // fp32 reduce-scatter result, or nullptr: re-read grads
     double *partials;           // 2 * grid_rs doubles
     DevStatus *status;
@@ -47,6 +48,10 @@ struct StepLaunch {
     double max_norm;
     int grid_rs;                // CTAs of the reduce-scatter + norm kernel
     int grid_update;            // CTAs of the update + all-gather kernel
+    // step variants (defaults: the pages' step)
+    bool moments_bf16 = false;  // m, v stored in bf16 (then m, v point at bf16 arrays)
+    bool decay_first = false;   // torch.optim.AdamW's order
+    double clip_eps = 0.0;      // c = min(1, max_norm / (norm + clip_eps))
 };
 
 // Enqueue the reduce-scatter + norm kernel, then the update + all-gather

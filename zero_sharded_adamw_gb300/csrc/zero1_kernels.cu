@@ -71,6 +71,7 @@ struct RsParams {
     int world;
     float inv_w;
     double max_norm;
+    double clip_eps;          // c = min(1, max_norm / (norm + clip_eps))
 };
 
 template <int CAP>
@@ -78,10 +79,12 @@ struct UpdParams {
     const uint16_t *grads[CAP];  // re-read mode only
     uint16_t *params[CAP];
     const float *ghat;           // spill mode only
-    float *master, *m, *v;
+    float *master;
+    void *m, *v;                 // fp32, or bf16 in the bf16-moment variant
     DevStatus *status;
     uint64_t nvec, n;
     int world;
+    int decay_first;             // torch.optim.AdamW's decay order
     StepScalars sc;
 };
 
@@ -315,8 +318,8 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
         if (p.max_norm > 0.0) {
             if (isnan(norm))
                 c = __int_as_float(0x7FC00000);
-            else if (norm > p.max_norm)
-                c = (float)(p.max_norm / norm);
+            else if (p.max_norm / (norm + p.clip_eps) < 1.0)
+                c = (float)(p.max_norm / (norm + p.clip_eps));
         }
         p.status->nsq = nsq;
         p.status->norm = norm;
@@ -328,16 +331,37 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 
 // ------------------------------------------------------------------- K2
 
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 // One parameter of the AdamW update, in the order the update is written.
-__device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, float &master, float &m, float &v)
+// MV16: the moments are bf16 tensors, so each operation on them rounds its
+// fp32 result to bf16.  decay_first: torch.optim.AdamW's order.
+template <bool MV16>
+__device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, bool decay_first, float &master,
+                                       float &m, float &v)
 {
     const float g = __fmul_rn(gh, c);
-    const float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, g));
-    const float vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(__fmul_rn(s.omb2, g), g));
-    const float d = __fadd_rn(__fsqrt_rn(vi), s.eps);
+    float mi, vi, d;
+    if (MV16) {
+        mi = bf16_round(__fmul_rn(s.beta1, m));
+        mi = bf16_round(__fadd_rn(mi, __fmul_rn(s.omb1, g)));
+        vi = bf16_round(__fmul_rn(s.beta2, v));
+        vi = bf16_round(__fadd_rn(vi, __fmul_rn(__fmul_rn(s.omb2, g), g)));
+        d = bf16_round(__fadd_rn(bf16_round(__fsqrt_rn(vi)), s.eps));
+    } else {
+        mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, g));
+        vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(__fmul_rn(s.omb2, g), g));
+        d = __fadd_rn(__fsqrt_rn(vi), s.eps);
+    }
     const float u = __fdiv_rn(mi, d);
-    float pm = __fsub_rn(master, __fmul_rn(s.step_size, u));
-    pm = __fmul_rn(pm, s.decay);
+    float pm = master;
+    if (decay_first) {
+        pm = __fmul_rn(pm, s.decay);
+        pm = __fsub_rn(pm, __fmul_rn(s.step_size, u));
+    } else {
+        pm = __fsub_rn(pm, __fmul_rn(s.step_size, u));
+        pm = __fmul_rn(pm, s.decay);
+    }
     master = pm;
     m = mi;
     v = vi;
@@ -345,6 +369,7 @@ __device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, 
 
 struct UpdSmem {
     float in[kStages][4][kTile];   // 128 KB: ghat (or the W <= 2 bf16 grads), master, m, v
+                                   // (m, v use half their slot when stored in bf16)
     uint16_t b16[kStages][kTile];  // 16 KB: the tile's bf16 parameters
     uint64_t full[kStages], done[kStages], empty[kStages];
     int abort;
@@ -352,8 +377,9 @@ struct UpdSmem {
 
 // Four consecutive parameters at offset o of stage s: AdamW in place on the
 // staged master, m, v and the bf16 values into the replica tile.
-template <bool REREAD>
-__device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc)
+template <bool REREAD, bool MV16>
+__device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc,
+                                        bool decay_first)
 {
     float gh[4];
     if (REREAD) {
@@ -380,16 +406,32 @@ __device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, 
         gh[3] = a.w;
     }
     float4 *w4 = reinterpret_cast<float4 *>(&sm.in[s][1][o]);
-    float4 *m4 = reinterpret_cast<float4 *>(&sm.in[s][2][o]);
-    float4 *v4 = reinterpret_cast<float4 *>(&sm.in[s][3][o]);
-    float4 w = *w4, m = *m4, v = *v4;
-    adamw1(gh[0], c, sc, w.x, m.x, v.x);
-    adamw1(gh[1], c, sc, w.y, m.y, v.y);
-    adamw1(gh[2], c, sc, w.z, m.z, v.z);
-    adamw1(gh[3], c, sc, w.w, m.w, v.w);
+    float4 w = *w4, m, v;
+    if (MV16) {
+        const uint2 rm = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(sm.in[s][2]) + o);
+        const uint2 rv = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(sm.in[s][3]) + o);
+        m = make_float4(__uint_as_float(rm.x << 16), __uint_as_float(rm.x & 0xFFFF0000u),
+                        __uint_as_float(rm.y << 16), __uint_as_float(rm.y & 0xFFFF0000u));
+        v = make_float4(__uint_as_float(rv.x << 16), __uint_as_float(rv.x & 0xFFFF0000u),
+                        __uint_as_float(rv.y << 16), __uint_as_float(rv.y & 0xFFFF0000u));
+    } else {
+        m = *reinterpret_cast<const float4 *>(&sm.in[s][2][o]);
+        v = *reinterpret_cast<const float4 *>(&sm.in[s][3][o]);
+    }
+    adamw1<MV16>(gh[0], c, sc, decay_first, w.x, m.x, v.x);
+    adamw1<MV16>(gh[1], c, sc, decay_first, w.y, m.y, v.y);
+    adamw1<MV16>(gh[2], c, sc, decay_first, w.z, m.z, v.z);
+    adamw1<MV16>(gh[3], c, sc, decay_first, w.w, m.w, v.w);
     *w4 = w;
-    *m4 = m;
-    *v4 = v;
+    if (MV16) {   // the values are bf16 already: the packing is exact
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(sm.in[s][2]) + o) =
+            make_uint2(pack2(m.x, m.y), pack2(m.z, m.w));
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(sm.in[s][3]) + o) =
+            make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+    } else {
+        *reinterpret_cast<float4 *>(&sm.in[s][2][o]) = m;
+        *reinterpret_cast<float4 *>(&sm.in[s][3][o]) = v;
+    }
     *reinterpret_cast<uint2 *>(&sm.b16[s][o]) = make_uint2(pack2(w.x, w.y), pack2(w.z, w.w));
 }
 
@@ -397,10 +439,11 @@ __device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, 
 // from the highest down (the reduce-scatter kernel wrote those last, so
 // they are the likeliest to still be in L2).  master, m, v are updated in
 // place in the stage and written back from there.
-template <int W, int CAP, bool REREAD>
+template <int W, int CAP, bool REREAD, bool MV16>
 __global__ void __launch_bounds__(kUpdThreads, 1)
 zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 {
+    constexpr uint32_t kMomBytes = MV16 ? 2u : 4u;   // bytes per stored moment
     extern __shared__ __align__(128) unsigned char smem_raw[];
     UpdSmem &sm = *reinterpret_cast<UpdSmem *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
@@ -433,7 +476,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
                 const uint64_t base = (uint64_t)j * kTile;
                 const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
                 const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
-                mbar_arrive_expect_tx(&sm.full[s], gbytes + 12u * cnt);
+                mbar_arrive_expect_tx(&sm.full[s], gbytes + 4u * cnt + 2u * kMomBytes * cnt);
                 if (REREAD) {
                     uint16_t *g = reinterpret_cast<uint16_t *>(sm.in[s][0]);
                     for (int r = 0; r < nw; ++r)
@@ -442,8 +485,10 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
                     tma_load_hint(sm.in[s][0], p.ghat + base, cnt * 4u, &sm.full[s], once);
                 }
                 tma_load_hint(sm.in[s][1], p.master + base, cnt * 4u, &sm.full[s], once);
-                tma_load_hint(sm.in[s][2], p.m + base, cnt * 4u, &sm.full[s], once);
-                tma_load_hint(sm.in[s][3], p.v + base, cnt * 4u, &sm.full[s], once);
+                tma_load_hint(sm.in[s][2], static_cast<const unsigned char *>(p.m) + base * kMomBytes,
+                              cnt * kMomBytes, &sm.full[s], once);
+                tma_load_hint(sm.in[s][3], static_cast<const unsigned char *>(p.v) + base * kMomBytes,
+                              cnt * kMomBytes, &sm.full[s], once);
             }
             if (*abort) drain_loads<kStages>(sm.full, k);
         }
@@ -461,9 +506,11 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             // Targets 0..2 are master, m, v; 3.. are the W replicas (the
             // all-gather).  Lane L issues targets L, L+32, ...
             for (int t = lane; t < nw + 3; t += 32) {
-                if (t < 3) {
-                    float *dst = t == 0 ? p.master : t == 1 ? p.m : p.v;
-                    tma_store_hint(dst + base, sm.in[s][1 + t], cnt * 4u, once);
+                if (t == 0) {
+                    tma_store_hint(p.master + base, sm.in[s][1], cnt * 4u, once);
+                } else if (t < 3) {
+                    unsigned char *dst = static_cast<unsigned char *>(t == 1 ? p.m : p.v);
+                    tma_store_hint(dst + base * kMomBytes, sm.in[s][1 + t], cnt * kMomBytes, once);
                 } else {
                     tma_store_hint(p.params[t - 3] + base, sm.b16[s], cnt * 2u, once);
                 }
@@ -497,8 +544,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             // line may hold the n % 8 tail and is left alone).
             discard_l2_line(p.ghat + base + threadIdx.x * 32u);
         }
-        if (o0 < cnt) update4<REREAD>(sm, s, o0, nw, c, p.sc);
-        if (o1 < cnt) update4<REREAD>(sm, s, o1, nw, c, p.sc);
+        if (o0 < cnt) update4<REREAD, MV16>(sm, s, o0, nw, c, p.sc, p.decay_first != 0);
+        if (o1 < cnt) update4<REREAD, MV16>(sm, s, o1, nw, c, p.sc, p.decay_first != 0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.done[s]);
@@ -508,11 +555,23 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     const uint64_t e = nel + threadIdx.x;
     if (blockIdx.x == 0 && threadIdx.x < kVec && e < p.n) {
         const float gh = REREAD ? __fmul_rn(rank_sum1(p.grads, nw, e), p.sc.inv_w) : p.ghat[e];
-        float w = p.master[e], m = p.m[e], v = p.v[e];
-        adamw1(gh, c, p.sc, w, m, v);
+        float w = p.master[e], m, v;
+        if (MV16) {
+            m = __uint_as_float((unsigned)static_cast<const uint16_t *>(p.m)[e] << 16);
+            v = __uint_as_float((unsigned)static_cast<const uint16_t *>(p.v)[e] << 16);
+        } else {
+            m = static_cast<const float *>(p.m)[e];
+            v = static_cast<const float *>(p.v)[e];
+        }
+        adamw1<MV16>(gh, c, p.sc, p.decay_first != 0, w, m, v);
         p.master[e] = w;
-        p.m[e] = m;
-        p.v[e] = v;
+        if (MV16) {
+            static_cast<__nv_bfloat16 *>(p.m)[e] = __float2bfloat16_rn(m);
+            static_cast<__nv_bfloat16 *>(p.v)[e] = __float2bfloat16_rn(v);
+        } else {
+            static_cast<float *>(p.m)[e] = m;
+            static_cast<float *>(p.v)[e] = v;
+        }
         const __nv_bfloat16 bw = __float2bfloat16_rn(w);
         for (int r = 0; r < nw; ++r) reinterpret_cast<__nv_bfloat16 *>(p.params[r])[e] = bw;
     }
@@ -544,6 +603,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     rp.world = s.world;
     rp.inv_w = s.sc.inv_w;
     rp.max_norm = s.max_norm;
+    rp.clip_eps = s.clip_eps;
 
     up.ghat = s.ghat;
     up.master = s.master;
@@ -554,11 +614,13 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     up.n = s.n;
     up.world = s.world;
     up.sc = s.sc;
+    up.decay_first = s.decay_first ? 1 : 0;
 
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
     auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
-    auto k2 = spill ? zero1_adamw_ag_kernel<W, CAP, false> : zero1_adamw_ag_kernel<W, CAP, true>;
+    auto k2 = spill ? (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, false, true> : zero1_adamw_ag_kernel<W, CAP, false, false>)
+                    : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true> : zero1_adamw_ag_kernel<W, CAP, true, false>);
     cudaError_t e;
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
     if ((e = allow_smem(k2, sizeof(UpdSmem))) != cudaSuccess) return e;
