@@ -378,6 +378,103 @@ def allreduce_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def zero2_arm(args, w: WL.Workload):
+    """The bucketed (ZeRO-2-style) step overlapped with an emulated backward.
+
+    The backward is emulated as, per bucket of P parameters (last layer
+    first), the two GEMMs a layer's backward runs on T tokens (2*T*P flops
+    each, bf16 on cuBLAS) on a compute stream; each bucket is handed to
+    zero1_bucket_reduce on a second stream as soon as its GEMMs finish, and
+    zero1_bucket_finish runs after the backward.  Reported: the backward
+    alone, backward + zero1_step back to back (the ZeRO-1 schedule), and the
+    overlapped schedule; the optimizer time left exposed after the backward
+    is the figure of merit."""
+    import zero_sharded_adamw_gb300 as z
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    hp = z.Hparams(**w.hparams())
+    grads = WL.grads(w, 1, dev)
+    reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
+    per_bucket = max(8, (int(args.bucket_mb * 1e6) // 2) // 8 * 8)
+    cuts = [(lo, min(per_bucket, w.n - lo)) for lo in range(0, w.n, per_bucket)][::-1]
+    d_model = 768
+    x = torch.randn(args.tokens, d_model, device=dev, dtype=torch.bfloat16)
+    mats = {cnt: torch.randn(d_model, max(128, cnt // d_model // 128 * 128), device=dev, dtype=torch.bfloat16)
+            for _, cnt in cuts}
+    opt = z.Zero1(w.n, w.world, hp, z.Options(bucket_ctas=args.bucket_ctas))
+    opt.set_state(WL.master(w, dev))
+    # Both streams are ordinary (non-default) streams: the legacy default
+    # stream would serialise against the other.
+    main = torch.cuda.Stream(dev)
+    comm = torch.cuda.Stream(dev, priority=-1)      # bucket reduces get SMs as soon as they free up
+
+    sleep_cycles = int(args.sleep_us * 1e-6 * 2.07e9)
+
+    def backward_bucket(cnt):
+        if args.backward == "sleep":            # a latency-bound backward that holds one SM
+            torch.cuda._sleep(sleep_cycles)
+            return None
+        y = x @ mats[cnt]                       # dgrad-sized GEMM
+        return y.t() @ x                        # wgrad-sized GEMM
+
+    def run(mode):
+        evs = []
+        for off, cnt in cuts:
+            backward_bucket(cnt)
+            if mode == "overlap":
+                ev = torch.cuda.Event()
+                ev.record(main)
+                evs.append((off, cnt, ev))
+        if mode == "seq":
+            opt.step(grads, reps, main)
+        elif mode == "overlap":
+            z.zero1_bucket_begin(opt.handle)
+            for off, cnt, ev in evs:
+                comm.wait_event(ev)
+                z.zero1_bucket_reduce(opt.handle, off, cnt, [g[off:off + cnt] for g in grads], comm)
+            main.wait_stream(comm)
+            z.zero1_bucket_finish(opt.handle, reps, main)
+
+    # Blackwell cuBLAS GEMMs are persistent and hold every SM until they end,
+    # so a backward leaves room for concurrent bucket reduces only if its
+    # GEMMs are told to leave SMs free (the same carve-out applies to all
+    # three schedules below).
+    carve = getattr(torch._C, "_set_sm_carveout_experimental", None)
+    carveout = args.bucket_ctas if (carve is not None and args.bucket_ctas > 0) else 0
+    if carveout:
+        carve(carveout)
+    out = {}
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(main):
+        for mode in ("bwd", "seq", "overlap"):
+            for _ in range(args.warmup):
+                run(mode)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for _ in range(args.steps):
+                run(mode)
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            out[mode] = e0.elapsed_time(e1) / args.steps
+    if carveout:
+        carve(None)
+    opt.close()
+    line = {
+        "metric": "ZeRO-2 bucketed step: optimizer ms exposed after an emulated backward", "value":
+            out["overlap"] - out["bwd"], "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world, "buckets": len(cuts),
+                   "bucket_params": per_bucket, "tokens": args.tokens, "bucket_ctas": args.bucket_ctas,
+                   "gemm_sm_carveout": carveout, "backward": args.backward,
+                   "sleep_us_per_bucket": args.sleep_us if args.backward == "sleep" else None},
+        "ms": {"backward_alone": out["bwd"], "backward_then_step": out["seq"], "overlapped": out["overlap"]},
+        "exposed_ms": {"zero1_schedule": out["seq"] - out["bwd"], "zero2_overlapped": out["overlap"] - out["bwd"]},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,8 +482,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="step", choices=["step", "allreduce"],
-                    help="step: the ZeRO-1 optimizer step (default); allreduce: the DDP all-reduce")
+    ap.add_argument("--path", default="step", choices=["step", "allreduce", "zero2"],
+                    help="step: the ZeRO-1 optimizer step (default); allreduce: the DDP all-reduce; "
+                         "zero2: the bucketed step overlapped with an emulated backward")
+    ap.add_argument("--bucket-mb", type=float, default=25.0, help="zero2: bucket size per rank (MB of bf16)")
+    ap.add_argument("--tokens", type=int, default=8192, help="zero2: tokens of the emulated backward")
+    ap.add_argument("--bucket-ctas", type=int, default=32, help="zero2: CTAs per bucket reduce (0 = one per SM)")
+    ap.add_argument("--backward", default="gemm", choices=["gemm", "sleep"],
+                    help="zero2: emulated backward: bf16 GEMMs, or a one-SM latency-bound kernel per bucket")
+    ap.add_argument("--sleep-us", type=float, default=240.0, help="zero2: sleep backward, microseconds per bucket")
     ap.add_argument("--ar-workload", default="lecture_fp32_w4", choices=sorted(WL.ALLREDUCE_WORKLOADS))
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
@@ -410,6 +514,8 @@ def main(argv=None):
                  else "working set fits in L2 (launch-latency bound)"}
     if args.path == "allreduce" and args.impl == "ours":
         allreduce_arm(args)
+    elif args.path == "zero2" and args.impl == "ours":
+        zero2_arm(args, w)
     elif args.impl == "reference":
         reference_arm(args, w, cfg)
     else:

@@ -108,17 +108,20 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     moment update computes in fp32 and rounds to bf16 per operation:
  *     m = bf16(bf16(b1*m) + (1-b1)*g), v = bf16(bf16(b2*v) + (1-b2)*g*g),
  *     d = bf16(bf16(sqrt(v)) + eps); the fp32 master update uses those.
+ *   bucket_ctas: CTAs of each zero1_bucket_reduce launch (0 = one per SM).
+ *     Fewer leave SMs to a backward running alongside on another stream.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
     int32_t decay_before_update;
     double clip_eps;
     int32_t moments_bf16;
+    int32_t bucket_ctas;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).
  * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
- * negative or non-finite clip_eps. */
+ * negative or non-finite clip_eps, a negative bucket_ctas. */
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
                     zero1_handle *out);
 
@@ -152,6 +155,34 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
  * allocates the staging buffers (4*W*n bytes) and creates those streams;
  * zero1_destroy frees both.  Errors as zero1_step, plus ZERO1_ENOMEM. */
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
+
+/* A ZeRO-2-style bucketed step ("Lecture 7 close reading", section 5.3:
+ * each layer's gradients are reduced to their owner as soon as the backward
+ * produces them and then freed; "Parallel training", "data parallel and
+ * ZeRO": buckets, and communication overlapped with the backward).  The
+ * same step as zero1_step, delivered in pieces:
+ *   zero1_bucket_begin(h): open a step.  The first call allocates the
+ *     bucket bookkeeping (64 KB) and, for W <= 2, an fp32 reduce-scatter
+ *     scratch of 4*W*S bytes.
+ *   zero1_bucket_reduce(h, offset, count, grad_ptrs, stream): reduce-scatter
+ *     parameters [offset, offset+count) -- grad_ptrs[r] points at rank r's
+ *     gradient for exactly that range (16-byte aligned; offset a multiple of
+ *     8) -- into the handle's fp32 scratch and record the range's norm
+ *     partial.  The gradient buffers may be reused once `stream` passes the
+ *     call.  Issue all of one step's buckets on one stream (they share
+ *     per-launch scratch); that stream may run alongside the caller's
+ *     backward on another.  At most 4096 buckets, in any order.
+ *   zero1_bucket_finish(h, param_ptrs, stream): the buckets must cover
+ *     [0, n) exactly once (else ZERO1_EINVAL and the step is abandoned);
+ *     forms the norm from the buckets' partials in call order, clips, runs
+ *     the AdamW + bf16 + all-gather kernel over all n, t -> t+1.
+ * The result equals zero1_step's for the same clip coefficient bit for bit;
+ * the norm itself is summed in a bucketing-dependent (but fixed) order.
+ * zero1_step is refused while a bucketed step is open. */
+int zero1_bucket_begin(zero1_handle h);
+int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs,
+                        void *stream);
+int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream);
 
 /* Checkpoint restore ("Parallel training", "training loop and checkpoint":
  * a checkpoint carries m, v and t).  master, m, v: arrays of n entries in

@@ -1,0 +1,156 @@
+"""The ZeRO-2-style bucketed step (zero1_bucket_begin / _reduce / _finish).
+
+Buckets arrive in backward order (last parameters first), each from its own
+small gradient buffers (the full gradient is never materialised), on a side
+stream.  With the GPU's clip coefficient injected the oracle's step must
+match bit for bit; the norm within 1e-6 of the oracle's.  With clipping off
+(c = 1 exactly on both paths) the bucketed step must equal zero1_step bit
+for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+import zero_sharded_adamw_gb300 as z
+from oracle import zero1_oracle as o
+from tests.gpu_util import bits_equal, f32, u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _buckets(n: int, rng, mean: int) -> list[tuple[int, int]]:
+    cuts, off = [], 0
+    while off < n:
+        size = int(rng.integers(1, 2 * mean)) * 8
+        cuts.append((off, min(size, n - off)))
+        off += size
+    return cuts[::-1]                      # backward order: last layers first
+
+
+def _bucketed_step(opt: z.Zero1, grads: list[torch.Tensor], reps, cuts, side: torch.cuda.Stream):
+    z.zero1_bucket_begin(opt.handle)
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    keep = []
+    with torch.cuda.stream(side):
+        for off, cnt in cuts:
+            bucket = [g[off:off + cnt].clone() for g in grads]     # the rank buckets of this layer
+            keep.append(bucket)
+            z.zero1_bucket_reduce(opt.handle, off, cnt, bucket, side)
+    main.wait_stream(side)
+    z.zero1_bucket_finish(opt.handle, reps, main)
+    torch.cuda.synchronize()
+
+
+def _state(opt: z.Zero1, n: int):
+    m = torch.empty(n, device="cuda")
+    mm, vv = torch.empty_like(m), torch.empty_like(m)
+    opt.get_state(m, mm, vv)
+    torch.cuda.synchronize()
+    return f32(m), f32(mm), f32(vv)
+
+
+@pytest.mark.parametrize("n,world,mean", [(1_000_003, 8, 4000), (65_541, 2, 300), (4099, 4, 37), (200_001, 64, 2000)])
+def test_bucketed_matches_oracle(n, world, mean):
+    w = WL.Workload("bk", n, world, 0.02, 3, max_norm=0.05)
+    d = w.hparams()
+    ohp = o.HP(**d)
+    rng = np.random.default_rng(n + world)
+    side = torch.cuda.Stream()
+    m0 = WL.master(w, "cuda")
+    reps = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    st = o.State(f32(m0))
+    with z.Zero1(n, world, z.Hparams(**d)) as opt:
+        opt.set_state(m0)
+        for t in range(1, 4):
+            grads = WL.grads(w, t, "cuda")
+            _bucketed_step(opt, grads, reps, _buckets(n, rng, mean), side)
+            norm, c = opt.grad_norm()
+            reps_o, norm_o, _ = o.step(st, [u16(g) for g in grads], ohp, clip_override=np.float32(c))
+            assert abs(norm - norm_o) <= 1e-6 * norm_o
+            master, m, v = _state(opt, n)
+            assert bits_equal(master, st.master) and bits_equal(m, st.m) and bits_equal(v, st.v)
+            for r in range(world):
+                assert np.array_equal(u16(reps[r]), reps_o[r])
+        assert opt.get_state() == 3
+
+
+def test_bucketed_equals_plain_step_without_clipping():
+    n, world = 777_777, 8
+    w = WL.Workload("eq", n, world, 0.02, 3, max_norm=0.0)
+    hp = z.Hparams(**w.hparams())
+    rng = np.random.default_rng(5)
+    side = torch.cuda.Stream()
+    m0 = WL.master(w, "cuda")
+    ra = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    rb = [torch.empty_like(ra[0]) for _ in range(world)]
+    with z.Zero1(n, world, hp) as a, z.Zero1(n, world, hp) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, 4):
+            grads = WL.grads(w, t, "cuda")
+            a.step(grads, ra)
+            _bucketed_step(b, grads, rb, _buckets(n, rng, 3000), side)
+        for x, y in zip(_state(a, n), _state(b, n)):
+            assert bits_equal(x, y)
+        assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+
+
+def test_bucketed_with_bf16_moments_and_torch_order():
+    n, world = 300_007, 4
+    w = WL.Workload("var", n, world, 0.02, 2, max_norm=0.05)
+    d = w.hparams()
+    opts = o.Options(decay_before_update=True, clip_eps=1e-6, moments_bf16=True)
+    rng = np.random.default_rng(9)
+    side = torch.cuda.Stream()
+    m0 = WL.master(w, "cuda")
+    reps = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    st = o.state_ex(f32(m0), opts)
+    with z.Zero1(n, world, z.Hparams(**d), z.Options(True, 1e-6, True)) as opt:
+        opt.set_state(m0)
+        for t in range(1, 3):
+            grads = WL.grads(w, t, "cuda")
+            _bucketed_step(opt, grads, reps, _buckets(n, rng, 1000), side)
+            _, c = opt.grad_norm()
+            reps_o, _, _ = o.step_ex(st, [u16(g) for g in grads], o.HP(**d), opts, clip_override=np.float32(c))
+            master = torch.empty(n, device="cuda")
+            m = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+            v = torch.empty_like(m)
+            opt.get_state(master, m, v)
+            torch.cuda.synchronize()
+            assert bits_equal(f32(master), st.master)
+            assert np.array_equal(u16(m), st.m) and np.array_equal(u16(v), st.v)
+            assert np.array_equal(u16(reps[0]), reps_o[0])
+
+
+def test_bucket_errors():
+    n, world = 1000, 2
+    g = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world) as opt:
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_reduce(opt.handle, 0, n, g)            # no open step
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_finish(opt.handle, g)
+        z.zero1_bucket_begin(opt.handle)
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_begin(opt.handle)                      # already open
+        with pytest.raises(z.Zero1Error):
+            opt.step(g, g)                                        # plain step refused while open
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_reduce(opt.handle, 4, 8, g)            # offset not a multiple of 8
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_reduce(opt.handle, 992, 16, g)         # past n
+        z.zero1_bucket_reduce(opt.handle, 0, 496, g)
+        z.zero1_bucket_reduce(opt.handle, 504, 496, g)            # gap at [496, 504)
+        with pytest.raises(z.Zero1Error) as e:
+            z.zero1_bucket_finish(opt.handle, g)
+        assert "exactly once" in str(e.value)
+        assert opt.get_state() == 0                               # abandoned: t unchanged
+        z.zero1_bucket_begin(opt.handle)                          # a fresh step can start
+        z.zero1_bucket_reduce(opt.handle, 0, 1000, g)
+        z.zero1_bucket_finish(opt.handle, g)
+        torch.cuda.synchronize()
+        assert opt.get_state() == 1

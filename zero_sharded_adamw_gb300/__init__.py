@@ -22,7 +22,7 @@ __all__ = [
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -47,6 +47,9 @@ _SIGS = {
     "zero1_set_lr": (_I32, [_P, _F64]),
     "zero1_get_grad_norm": (_I32, [_P, _P, _P, _P]),
     "zero1_layout": (_I32, [_P, _P, _P, _P]),
+    "zero1_bucket_begin": (_I32, [_P]),
+    "zero1_bucket_reduce": (_I32, [_P, _U64, _U64, _P, _P]),
+    "zero1_bucket_finish": (_I32, [_P, _P, _P]),
     "zero1_profile_start": (_I32, [_P, _I32]),
     "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
     "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
@@ -84,7 +87,7 @@ class Hparams:
 
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
-                ("moments_bf16", C.c_int32)]
+                ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32)]
 
 
 @dataclass
@@ -94,10 +97,11 @@ class Options:
     decay_before_update: bool = False
     clip_eps: float = 0.0
     moments_bf16: bool = False
+    bucket_ctas: int = 0
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
-                         1 if self.moments_bf16 else 0)
+                         1 if self.moments_bf16 else 0, self.bucket_ctas)
 
 
 _lib = None
@@ -220,6 +224,20 @@ def zero1_layout(h: int) -> tuple[int, int, int]:
     s, p, b = C.c_uint64(), C.c_uint64(), C.c_uint64()
     _check(_load().zero1_layout(h, C.byref(s), C.byref(p), C.byref(b)))
     return s.value, p.value, b.value
+
+
+def zero1_bucket_begin(h: int) -> None:
+    _check(_load().zero1_bucket_begin(h))
+
+
+def zero1_bucket_reduce(h: int, offset: int, count: int, grad_ptrs, stream=None) -> None:
+    """Reduce-scatter one bucket: grad_ptrs[r] holds rank r's gradient for
+    parameters [offset, offset+count)."""
+    _check(_load().zero1_bucket_reduce(h, offset, count, _ptrs(grad_ptrs), _stream(stream)))
+
+
+def zero1_bucket_finish(h: int, param_ptrs, stream=None) -> None:
+    _check(_load().zero1_bucket_finish(h, _ptrs(param_ptrs), _stream(stream)))
 
 
 def zero1_profile_start(h: int, capacity: int) -> None:

@@ -20,6 +20,8 @@
 #include <mutex>
 #include <new>
 #include <unordered_set>
+#include <algorithm>
+#include <utility>
 #include <vector>
 
 #include "zero1.h"
@@ -54,7 +56,15 @@ struct zero1_ctx {
     // per-kernel timing (zero1_profile_start/stop): 3 events per step
     std::vector<cudaEvent_t> prof;
     int prof_capacity = 0, prof_used = 0;
+    // bucketed step (zero1_bucket_*): buckets in call order, their norm sums,
+    // and a reduce-scatter scratch for W <= 2 (whose plain step re-reads)
+    bool bucket_open = false;
+    std::vector<std::pair<uint64_t, uint64_t>> buckets;
+    double *bucket_sums = nullptr;
+    float *ghat_bucket = nullptr;
 };
+
+constexpr int kMaxBuckets = 4096;
 
 namespace {
 
@@ -165,6 +175,7 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
     if (opts) {
         if (opts->size != sizeof(zero1_options)) return fail(ZERO1_EINVAL, "opts->size must be sizeof(zero1_options)");
         if (!finite_nonneg(opts->clip_eps)) return fail(ZERO1_EINVAL, "clip_eps must be finite and >= 0");
+        if (opts->bucket_ctas < 0) return fail(ZERO1_EINVAL, "bucket_ctas must be >= 0");
         o = *opts;
     }
 
@@ -236,6 +247,8 @@ int zero1_destroy(zero1_handle h)
     cudaError_t e1 = cudaDeviceSynchronize();
     cudaError_t e2 = cudaFree(h->block);
     cudaError_t e3 = h->staging ? cudaFree(h->staging) : cudaSuccess;
+    if (h->bucket_sums) cudaFree(h->bucket_sums);
+    if (h->ghat_bucket) cudaFree(h->ghat_bucket);
     for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
     if (h->copy_ready) {
         for (int i = 0; i < 4; ++i) {
@@ -254,6 +267,7 @@ int zero1_destroy(zero1_handle h)
 int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_ptrs, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (h->bucket_open) return fail(ZERO1_EINVAL, "a bucketed step is open; finish it first");
     if (!grad_ptrs || !param_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
     for (int r = 0; r < h->world; ++r) {
         if (!grad_ptrs[r] || !param_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
@@ -507,6 +521,116 @@ int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, ui
     if (rs_norm_ms) *rs_norm_ms = a;
     if (update_ms) *update_ms = b;
     if (steps) *steps = used;
+    return ZERO1_OK;
+}
+
+int zero1_bucket_begin(zero1_handle h)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (h->bucket_open) return fail(ZERO1_EINVAL, "a bucketed step is already open");
+    DeviceGuard g(h->device);
+    cudaError_t e;
+    if (!h->bucket_sums &&
+        (e = cudaMalloc(&h->bucket_sums, 2 * sizeof(double) * kMaxBuckets)) != cudaSuccess) {
+        h->bucket_sums = nullptr;
+        return cuda_fail(e, "cudaMalloc of bucket sums");
+    }
+    if (!h->ghat && !h->ghat_bucket &&
+        (e = cudaMalloc(&h->ghat_bucket, round_up(h->padded * sizeof(float), 256))) != cudaSuccess) {
+        h->ghat_bucket = nullptr;
+        return cuda_fail(e, "cudaMalloc of the reduce-scatter scratch");
+    }
+    h->buckets.clear();
+    h->bucket_open = true;
+    return ZERO1_OK;
+}
+
+int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!h->bucket_open) return fail(ZERO1_EINVAL, "no bucketed step is open (call zero1_bucket_begin)");
+    if (count == 0 || offset > h->n || count > h->n - offset)
+        return fail(ZERO1_EINVAL, "bucket [%llu, +%llu) is outside [0, n)", (unsigned long long)offset,
+                    (unsigned long long)count);
+    if (offset % zero1::kVec) return fail(ZERO1_EINVAL, "bucket offsets must be multiples of 8");
+    if ((int)h->buckets.size() >= kMaxBuckets) return fail(ZERO1_EINVAL, "more than %d buckets", kMaxBuckets);
+    if (!grad_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r) {
+        if (!grad_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
+        if (!aligned16(grad_ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+    }
+    DeviceGuard g(h->device);
+    zero1::StepLaunch s;
+    s.grads = grad_ptrs;
+    s.params = nullptr;
+    s.world = h->world;
+    s.n = count;
+    s.master = h->master;
+    s.m = h->m;
+    s.v = h->v;
+    s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    s.clip_eps = h->opts.clip_eps;
+    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    if (h->opts.bucket_ctas > 0 && s.grid_rs > h->opts.bucket_ctas) s.grid_rs = h->opts.bucket_ctas;
+    s.phase = 1;
+    s.bucket_sums = h->bucket_sums;
+    s.bucket_index = (int)h->buckets.size();
+    cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    h->buckets.emplace_back(offset, count);
+    return ZERO1_OK;
+}
+
+int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!h->bucket_open) return fail(ZERO1_EINVAL, "no bucketed step is open");
+    if (!param_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r) {
+        if (!param_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
+        if (!aligned16(param_ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+    }
+    std::vector<std::pair<uint64_t, uint64_t>> sorted = h->buckets;
+    std::sort(sorted.begin(), sorted.end());
+    uint64_t next = 0;
+    for (const auto &b : sorted) {
+        if (b.first != next) break;
+        next = b.first + b.second;
+    }
+    if (next != h->n) {
+        h->bucket_open = false;
+        return fail(ZERO1_EINVAL, "the buckets must cover [0, n) exactly once; the bucketed step is abandoned");
+    }
+    DeviceGuard g(h->device);
+    zero1::StepLaunch s;
+    s.grads = nullptr;
+    s.params = param_ptrs;
+    s.world = h->world;
+    s.n = h->n;
+    s.master = h->master;
+    s.m = h->m;
+    s.v = h->v;
+    s.ghat = h->ghat ? h->ghat : h->ghat_bucket;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    s.grid_rs = h->grid_rs;
+    s.grid_update = h->grid_update;
+    s.moments_bf16 = h->opts.moments_bf16 != 0;
+    s.decay_first = h->opts.decay_before_update != 0;
+    s.clip_eps = h->opts.clip_eps;
+    s.phase = 2;
+    s.bucket_sums = h->bucket_sums;
+    s.nbuckets = (int)h->buckets.size();
+    cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    h->bucket_open = false;
+    h->t += 1;
     return ZERO1_OK;
 }
 

@@ -52,6 +52,11 @@ struct StepLaunch {
     bool moments_bf16 = false;  // m, v stored in bf16 (then m, v point at bf16 arrays)
     bool decay_first = false;   // torch.optim.AdamW's order
     double clip_eps = 0.0;      // c = min(1, max_norm / (norm + clip_eps))
+    // bucketed (ZeRO-2 style) step
+    int phase = 0;                  // 0: both kernels, 1: reduce-scatter only, 2: update only
+    double *bucket_sums = nullptr;  // phase 1: written at [2*bucket_index]; phase 2: read
+    int bucket_index = 0;
+    int nbuckets = 0;
 };
 
 // Enqueue the reduce-scatter + norm kernel, then the update + all-gather

@@ -72,6 +72,8 @@ struct RsParams {
     float inv_w;
     double max_norm;
     double clip_eps;          // c = min(1, max_norm / (norm + clip_eps))
+    double *bucket_sums;      // bucketed step: this launch's (sum, plain sum) go to
+    int bucket;               // bucket_sums[2*bucket .. +1] instead of forming c
 };
 
 template <int CAP>
@@ -86,6 +88,9 @@ struct UpdParams {
     int world;
     int decay_first;             // torch.optim.AdamW's decay order
     StepScalars sc;
+    const double *bucket_sums;   // bucketed step: c comes from these nbuckets pairs
+    int nbuckets;
+    double max_norm, clip_eps;
 };
 
 // Scalar rank-ordered sum for the last n % 8 parameters.
@@ -146,6 +151,30 @@ __device__ __forceinline__ void consumer_sum2(double &a, double &b, double *sa, 
         }
     }
     consumer_sync();
+}
+
+// The norm and clip coefficient from the sum of squares `x` and its
+// uncompensated companion `y` (which carries inf/NaN): c = min(1,
+// max_norm/(norm + clip_eps)) when clipping is on, NaN for a NaN norm.
+__device__ __forceinline__ void finish_norm(double x, double y, double max_norm, double clip_eps, DevStatus *status,
+                                            float *clip_out)
+{
+    const double nsq = isfinite(y) ? x : y;
+    const double norm = sqrt(nsq);
+    float c = 1.0f;
+    if (max_norm > 0.0) {
+        if (isnan(norm))
+            c = __int_as_float(0x7FC00000);
+        else if (max_norm / (norm + clip_eps) < 1.0)
+            c = (float)(max_norm / (norm + clip_eps));
+    }
+    if (status) {
+        status->nsq = nsq;
+        status->norm = norm;
+        status->clip = c;
+        status->flags = isfinite(norm) ? 0u : kFlagNonFinite;
+    }
+    *clip_out = c;
 }
 
 // ------------------------------------------------------------------- K1
@@ -312,19 +341,13 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
     }
     consumer_sum2(x, y, sm.red_a, sm.red_b);
     if (threadIdx.x == 0) {
-        const double nsq = isfinite(y) ? x : y;
-        const double norm = sqrt(nsq);
-        float c = 1.0f;
-        if (p.max_norm > 0.0) {
-            if (isnan(norm))
-                c = __int_as_float(0x7FC00000);
-            else if (p.max_norm / (norm + p.clip_eps) < 1.0)
-                c = (float)(p.max_norm / (norm + p.clip_eps));
+        if (p.bucket_sums) {            // one bucket of a bucketed step
+            p.bucket_sums[2 * p.bucket] = x;
+            p.bucket_sums[2 * p.bucket + 1] = y;
+        } else {
+            float c;
+            finish_norm(x, y, p.max_norm, p.clip_eps, p.status, &c);
         }
-        p.status->nsq = nsq;
-        p.status->norm = norm;
-        p.status->clip = c;
-        p.status->flags = isfinite(norm) ? 0u : kFlagNonFinite;
         p.status->ticket = 0u;
     }
 }
@@ -373,6 +396,7 @@ struct UpdSmem {
     uint16_t b16[kStages][kTile];  // 16 KB: the tile's bf16 parameters
     uint64_t full[kStages], done[kStages], empty[kStages];
     int abort;
+    float clip;
 };
 
 // Four consecutive parameters at offset o of stage s: AdamW in place on the
@@ -460,6 +484,18 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             mbar_init(&sm.empty[s], 1);
         }
         sm.abort = 0;
+        if (p.bucket_sums) {
+            // Bucketed step: every CTA forms c from the buckets' sums in
+            // call order (the same value everywhere); CTA 0 records it.
+            double x = 0.0, y = 0.0;
+            for (int b = 0; b < p.nbuckets; ++b) {
+                x += p.bucket_sums[2 * b];
+                y += p.bucket_sums[2 * b + 1];
+            }
+            finish_norm(x, y, p.max_norm, p.clip_eps, blockIdx.x == 0 ? p.status : nullptr, &sm.clip);
+        } else {
+            sm.clip = p.status->clip;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -529,7 +565,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     // Consumers: thread t owns parameters [4t, 4t+4) and [1024+4t, 1024+4t+4)
     // of every tile, so a warp's 16-byte shared-memory accesses are
     // consecutive (no bank conflicts).
-    const float c = p.status->clip;
+    const float c = sm.clip;
     const uint32_t o0 = threadIdx.x * 4u, o1 = kTile / 2 + threadIdx.x * 4u;
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
@@ -591,9 +627,9 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     RsParams<CAP> rp{};
     UpdParams<CAP> up{};
     for (int r = 0; r < s.world; ++r) {
-        rp.grads[r] = static_cast<const uint16_t *>(s.grads[r]);
-        up.grads[r] = static_cast<const uint16_t *>(s.grads[r]);
-        up.params[r] = static_cast<uint16_t *>(s.params[r]);
+        rp.grads[r] = s.grads ? static_cast<const uint16_t *>(s.grads[r]) : nullptr;
+        up.grads[r] = s.grads ? static_cast<const uint16_t *>(s.grads[r]) : nullptr;
+        up.params[r] = s.params ? static_cast<uint16_t *>(s.params[r]) : nullptr;
     }
     rp.ghat = s.ghat;
     rp.partials = s.partials;
@@ -604,6 +640,8 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     rp.inv_w = s.sc.inv_w;
     rp.max_norm = s.max_norm;
     rp.clip_eps = s.clip_eps;
+    rp.bucket_sums = s.bucket_sums;
+    rp.bucket = s.bucket_index;
 
     up.ghat = s.ghat;
     up.master = s.master;
@@ -615,6 +653,10 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     up.world = s.world;
     up.sc = s.sc;
     up.decay_first = s.decay_first ? 1 : 0;
+    up.bucket_sums = s.bucket_sums;
+    up.nbuckets = s.nbuckets;
+    up.max_norm = s.max_norm;
+    up.clip_eps = s.clip_eps;
 
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
@@ -625,11 +667,15 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
     if ((e = allow_smem(k2, sizeof(UpdSmem))) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    k1<<<s.grid_rs, kRsThreads, sizeof(RsSmem), stream>>>(rp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (s.phase != 2) {
+        k1<<<s.grid_rs, kRsThreads, sizeof(RsSmem), stream>>>(rp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-    k2<<<s.grid_update, kUpdThreads, sizeof(UpdSmem), stream>>>(up);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (s.phase != 1) {
+        k2<<<s.grid_update, kUpdThreads, sizeof(UpdSmem), stream>>>(up);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }
