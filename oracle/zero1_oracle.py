@@ -75,6 +75,7 @@ def _signatures():
         "zref_step_ex": (None, [u64, i32, P, P, u64, P, P, P, P, P, P, i32, f32, P, P]),
         "zref_allreduce_f32_direct": (None, [P, i32, u64, i32, P]),
         "zref_allreduce_f32_rs_ag": (None, [P, i32, u64, i32, P, P]),
+        "zref_all_gather_shards": (None, [C.c_size_t, P, i32, u64, u64, P]),
         "zref_zero_bytes_per_rank": (f64, [i32, f64, i32, f64]),
         "zref_ring_send_bytes": (f64, [f64, i32, i32]),
     }
@@ -360,6 +361,17 @@ def allreduce_f32_rs_ag(inputs, average: bool = False):
     lib().zref_allreduce_f32_rs_ag(_ptr_array(inputs), len(inputs), n, 1 if average else 0,
                                    _ptr(scratch), _ptr_array(outs))
     return outs, scratch
+
+
+def all_gather_shards(shards, n: int, shard_len: int):
+    """Rank r's shard holds elements [r*S, min((r+1)*S, n)); returns the W
+    gathered n-element outputs (same dtype as the shards)."""
+    shards = [np.ascontiguousarray(s) for s in shards]
+    dt = shards[0].dtype
+    outs = [np.empty(n, dtype=dt) for _ in shards]
+    keep = [s if s.size else np.empty(1, dtype=dt) for s in shards]
+    lib().zref_all_gather_shards(dt.itemsize, _ptr_array(keep), len(shards), n, shard_len, _ptr_array(outs))
+    return outs
 
 
 def zero_bytes_per_rank(stage: int, psi: float, world: int, k: float = 12.0) -> float:

@@ -502,6 +502,26 @@ void zref_allreduce_f32_rs_ag(const float *const *in, int world, uint64_t n, int
     }
 }
 
+/* All-gather of shards ("Parallel training", "How cards talk: collective
+ * communication": every rank receives the concatenation of all ranks'
+ * pieces; "Lecture 7 close reading" 5.4: ZeRO-3 gathers each layer's
+ * sharded parameters before using them).  Rank r holds elements
+ * [r*S, min((r+1)*S, n)) of an n-element buffer, elem_size bytes each;
+ * every output q receives all n elements.  A byte copy: no arithmetic. */
+void zref_all_gather_shards(size_t elem_size, const void *const *shards, int world, uint64_t n,
+                            uint64_t shard_len, void *const *outs)
+{
+    for (int q = 0; q < world; ++q) {
+        for (int r = 0; r < world; ++r) {
+            uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len;
+            if (lo > n) lo = n;
+            if (hi > n) hi = n;
+            if (hi > lo)
+                memcpy((char *)outs[q] + lo * elem_size, shards[r], (size_t)(hi - lo) * elem_size);
+        }
+    }
+}
+
 /* ------------------------------------------------------- accounting */
 
 /* Per-rank bytes of parameter-related memory (PT "data parallel and ZeRO";

@@ -126,6 +126,34 @@ def pin_allreduce_f32_rank_order():
                 assert np.array_equal(via[q].view(np.uint32), want.view(np.uint32)), (world, average)
 
 
+def pin_all_gather_shards():
+    """The printed example's last column: the reduce-scatter outputs [6],
+    [10], [14], [18] all-gathered give [6, 10, 14, 18] on every rank; for
+    random ragged shards the gather equals numpy's concatenation; and a
+    reduce-scatter (sum) followed by this gather equals the all-reduce
+    written directly, bit for bit."""
+    g = golden("collectives_4rank.txt")
+    world = int(g["world"][0][0])
+    shards = [np.array([float(v)], np.float32) for _, v in sorted((int(r), v) for r, v in g["reduce_scatter"])]
+    outs = o.all_gather_shards(shards, world, 1)
+    want = np.array(g["all_gather"][0], np.float32)
+    assert all(np.array_equal(x, want) for x in outs)
+    rng = np.random.default_rng(13)
+    for n, world, extra in ((1000, 3, 0), (1000, 8, 5), (17, 4, 0), (5, 8, 0)):
+        s = -(-n // world) + extra
+        full = rng.integers(0, 65535, n).astype(np.uint16)
+        sh = [full[min(r * s, n):min((r + 1) * s, n)] for r in range(world)]
+        outs = o.all_gather_shards(sh, n, s)
+        assert all(np.array_equal(x, np.concatenate(sh)) for x in outs)
+    x = [rand_bf16(rng, 1001, 1.0) for _ in range(5)]
+    _, rs = o.allreduce_rs_ag(x)                       # fp32 reduce-scatter slices
+    s = o.shard_len(1001, 5)
+    b16 = o.f32_to_bf16(rs)
+    gathered = o.all_gather_shards([b16[r * s:(r + 1) * s] for r in range(5)], 1001, s)
+    direct = o.allreduce_sum_direct(x)
+    assert all(np.array_equal(a, b) for a, b in zip(gathered, direct))
+
+
 def pin_rs_rank_order():
     """The reduce-scatter sum is an fp32 left fold in rank order (numpy's
     sequential float32 cumsum) scaled by fp32(1/W); ragged n included."""

@@ -49,6 +49,8 @@ MUTANTS = {
     "variant_decay_order_ignored": ("        if (o->decay_before_update) {", "        if (0) {"),
     "variant_clip_eps_ignored": ("    double q = max_norm / (norm + clip_eps);", "    double q = max_norm / norm;"),
     "variant_bf16_v_not_stored": ("            vb[i] = zref_f32_to_bf16(vi);", "            (void)vb;"),
+    "gather_shards_off_by_one": ("uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len;",
+                                 "uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len - 1;"),
     "stage1_not_sharded": ("case 1: return (2.0 + 2.0) * psi + k * psi / w;", "case 1: return (2.0 + 2.0 + k) * psi;"),
     "ring_missing_factor": ("return op == 0 ? 2.0 * one : one;", "return one;"),
 }
