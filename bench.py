@@ -475,6 +475,112 @@ def zero2_arm(args, w: WL.Workload):
     print(json.dumps(line), flush=True)
 
 
+def fsdp_arm(args):
+    """ZeRO-3 / FSDP forward over the GPT-2-small layers (embeddings + 12
+    blocks), W = 8 emulated ranks: each layer's bf16 parameters are sharded
+    and all-gathered (zero1_allgather) onto every rank before the layer
+    runs.  Schedules: compute alone; gather then compute, layer by layer;
+    and prefetch -- layer l+1's gather on a side stream while layer l
+    computes, into the other of two staging sets.  The layer compute is
+    emulated by a one-SM latency-bound kernel (args.layer_us per layer) or
+    by bf16 GEMMs on args.tokens tokens."""
+    import zero_sharded_adamw_gb300 as z
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    world = 8
+    shapes = WL.gpt2_small_shapes()
+    sizes = [shapes[0][0] * shapes[0][1] + shapes[1][0] * shapes[1][1]]
+    for b in range(12):
+        blk = shapes[2 + 8 * b: 10 + 8 * b]
+        sizes.append(sum(int(torch.tensor(s).prod()) for s in blk))
+    layers = []
+    g = torch.Generator(device=dev).manual_seed(77)
+    for p in sizes:
+        s = -(-(-(-p // world)) // 8) * 8
+        shards = [torch.randn(max(0, min(s, p - r * s)), generator=g, device=dev).to(torch.bfloat16)
+                  for r in range(world)]
+        layers.append((p, s, shards))
+    pmax = max(sizes)
+    staging = [[torch.empty(pmax, dtype=torch.bfloat16, device=dev) for _ in range(world)] for _ in range(2)]
+    x = torch.randn(args.tokens, 768, device=dev, dtype=torch.bfloat16)
+    mats = [torch.randn(768, max(128, p // 768 // 128 * 128), device=dev, dtype=torch.bfloat16) for p in sizes]
+    sleep_cycles = int(args.layer_us * 1e-6 * 2.07e9)
+    main, side = torch.cuda.Stream(dev), torch.cuda.Stream(dev, priority=-1)
+
+    def compute(l):
+        if args.backward == "sleep":
+            torch.cuda._sleep(sleep_cycles)
+        else:
+            y = x @ mats[l]
+            y.t() @ x
+
+    def gather(l, buf, stream):
+        p, s, shards = layers[l]
+        z.zero1_allgather(p, world, s, z.DTYPE_BF16, [t if t.numel() else None for t in shards],
+                          staging[buf], None, stream)
+
+    def run(mode):
+        if mode == "compute":
+            for l in range(len(layers)):
+                compute(l)
+        elif mode == "gather":
+            for l in range(len(layers)):
+                gather(l, l % 2, main)
+        elif mode == "seq":
+            for l in range(len(layers)):
+                gather(l, l % 2, main)
+                compute(l)
+        else:
+            done = [torch.cuda.Event() for _ in layers]
+            used = [torch.cuda.Event() for _ in layers]
+            side.wait_stream(main)
+            gather(0, 0, side)
+            done[0].record(side)
+            for l in range(len(layers)):
+                if l + 1 < len(layers):
+                    if l >= 1:
+                        side.wait_event(used[l - 1])          # staging set (l+1)%2 is free
+                    gather(l + 1, (l + 1) % 2, side)
+                    done[l + 1].record(side)
+                main.wait_event(done[l])
+                compute(l)
+                used[l].record(main)
+
+    out = {}
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(main):
+        for mode in ("compute", "gather", "seq", "prefetch"):
+            for _ in range(args.warmup):
+                run(mode)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for _ in range(args.steps):
+                run(mode)
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            out[mode] = e0.elapsed_time(e1) / args.steps
+    total = sum(sizes)
+    ag_bytes = (1 + world) * 2 * total          # read every shard once, write W full copies
+    peak, peak_kind = measured_peak()
+    gbs = ag_bytes / (out["gather"] / 1e3) / 1e9
+    line = {
+        "metric": "FSDP forward: per-layer all-gather ms exposed, gather then compute vs prefetch",
+        "value": out["prefetch"] - out["compute"], "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "gpt2_small layers (embeddings + 12 blocks)", "n_params": total,
+                   "emulated_ranks": world, "layers": len(sizes), "compute": args.backward,
+                   "layer_us": args.layer_us if args.backward == "sleep" else None, "tokens": args.tokens},
+        "ms": out,
+        "exposed_ms": {"gather_then_compute": out["seq"] - out["compute"],
+                       "prefetch": out["prefetch"] - out["compute"]},
+        "allgather": {"gbs": gbs, "peak": peak, "frac": gbs / peak, "peak_kind": peak_kind,
+                      "bytes_per_forward": ag_bytes, "gpu_launches_per_forward": len(sizes)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,15 +588,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="step", choices=["step", "allreduce", "zero2"],
+    ap.add_argument("--path", default="step", choices=["step", "allreduce", "zero2", "fsdp"],
                     help="step: the ZeRO-1 optimizer step (default); allreduce: the DDP all-reduce; "
-                         "zero2: the bucketed step overlapped with an emulated backward")
+                         "zero2: the bucketed step overlapped with an emulated backward; "
+                         "fsdp: per-layer parameter all-gather with prefetch")
     ap.add_argument("--bucket-mb", type=float, default=25.0, help="zero2: bucket size per rank (MB of bf16)")
     ap.add_argument("--tokens", type=int, default=8192, help="zero2: tokens of the emulated backward")
     ap.add_argument("--bucket-ctas", type=int, default=32, help="zero2: CTAs per bucket reduce (0 = one per SM)")
     ap.add_argument("--backward", default="gemm", choices=["gemm", "sleep"],
                     help="zero2: emulated backward: bf16 GEMMs, or a one-SM latency-bound kernel per bucket")
     ap.add_argument("--sleep-us", type=float, default=240.0, help="zero2: sleep backward, microseconds per bucket")
+    ap.add_argument("--layer-us", type=float, default=150.0, help="fsdp: sleep compute, microseconds per layer")
     ap.add_argument("--ar-workload", default="lecture_fp32_w4", choices=sorted(WL.ALLREDUCE_WORKLOADS))
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
@@ -516,6 +624,8 @@ def main(argv=None):
         allreduce_arm(args)
     elif args.path == "zero2" and args.impl == "ours":
         zero2_arm(args, w)
+    elif args.path == "fsdp" and args.impl == "ours":
+        fsdp_arm(args)
     elif args.impl == "reference":
         reference_arm(args, w, cfg)
     else:

@@ -302,6 +302,21 @@ int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp, uint64_t 
 int zero1_allreduce(uint64_t n, int world, int dtype, int op, const void *const *in_ptrs,
                     void *const *out_ptrs, unsigned *errors, void *stream);
 
+/* The ZeRO-3 / FSDP parameter all-gather ("Lecture 7 close reading:
+ * Parallelism (part 1)", section 5.4: before a layer runs, its sharded
+ * parameters are all-gathered onto every rank; "Parallel training", "How
+ * cards talk: collective communication": all-gather concatenates every
+ * rank's piece onto all ranks).  Rank r's shard_ptrs[r] holds elements
+ * [r*S, min((r+1)*S, n)) of an n-element buffer (S = shard_len, a multiple
+ * of 8, S*W >= n; ranks past n hold nothing and may pass any pointer);
+ * every out_ptrs[q] receives all n elements.  A byte copy, bf16 or fp32.
+ * In place is allowed: shard_ptrs[r] may be out_ptrs[r] + r*S elements.
+ * Buffers 16-byte aligned; `errors` as zero1_allreduce.  Asynchronous on
+ * `stream`; allocates nothing; one kernel launch.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_allgather(uint64_t n, int world, uint64_t shard_len, int dtype, const void *const *shard_ptrs,
+                    void *const *out_ptrs, unsigned *errors, void *stream);
+
 /* Message for the last error on this thread ("" if none). */
 const char *zero1_last_error(void);
 

@@ -22,7 +22,7 @@ __all__ = [
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -56,6 +56,7 @@ _SIGS = {
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
     "zero1_allreduce": (_I32, [_U64, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "zero1_allgather": (_I32, [_U64, _I32, _U64, _I32, _P, _P, _P, _P]),
     "zero1_last_error": (C.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -284,6 +285,13 @@ def zero1_allreduce(n: int, world: int, dtype: int, op: int, in_ptrs, out_ptrs, 
     """DDP all-reduce of W device buffers (bf16 or fp32, sum or mean)."""
     _check(_load().zero1_allreduce(n, world, dtype, op, _ptrs(in_ptrs), _ptrs(out_ptrs), _addr(errors),
                                    _stream(stream)))
+
+
+def zero1_allgather(n: int, world: int, shard_len: int, dtype: int, shard_ptrs, out_ptrs, errors=None,
+                    stream=None) -> None:
+    """ZeRO-3 parameter all-gather: rank r's shard holds [r*S, min((r+1)*S, n))."""
+    _check(_load().zero1_allgather(n, world, shard_len, dtype, _ptrs(shard_ptrs), _ptrs(out_ptrs),
+                                   _addr(errors), _stream(stream)))
 
 
 class Zero1:

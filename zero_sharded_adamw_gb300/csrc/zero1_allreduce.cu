@@ -319,6 +319,126 @@ cudaError_t launch_ar_t(uint64_t n, int world, int average, const void *const *i
     return launch_ar<T, 512>(n, world, average, in, out, errors, num_sms, stream);
 }
 
+// ------------------------------------------------------------ all-gather
+
+// The ZeRO-3 / FSDP parameter all-gather ("Lecture 7 close reading" 5.4:
+// before a layer runs, its sharded parameters are gathered onto every rank).
+// Rank r's shard holds elements [r*S, min((r+1)*S, n)); every output q
+// receives all n.  A byte copy with W-way fan-out.  One 32-thread CTA per
+// 16 KB tile: lane 0 bulk-loads the tile into shared memory, the lanes
+// bulk-store it to the W outputs, the CTA waits for the stores to have read
+// shared memory and exits.  Per-layer gathers are short, so instead of a
+// persistent pipeline many small CTAs (about 13 per SM) keep ~200 KB per
+// SM in flight.  The last CTA copies every shard's sub-16-byte tail.
+constexpr int kAgBytes = 16384;
+
+template <int CAP>
+struct AgParams {
+    const unsigned char *shards[CAP];
+    unsigned char *out[CAP];
+    unsigned *errors;
+    uint64_t n, shard_len;
+    uint64_t tiles_per_shard;
+    int world;
+    int esize;
+};
+
+struct AgSmem {
+    unsigned char tile[kAgBytes];
+    uint64_t full;
+};
+
+// Elements of shard r, and of its 16-byte vector part.
+__device__ __forceinline__ void shard_extent(uint64_t n, uint64_t s, int r, int esize, uint64_t &len, uint64_t &vlen)
+{
+    const uint64_t lo = (uint64_t)r * s;
+    len = lo >= n ? 0 : (n - lo < s ? n - lo : s);
+    const uint64_t per16 = 16u / (uint64_t)esize;
+    vlen = len / per16 * per16;
+}
+
+template <int CAP>
+__global__ void __launch_bounds__(32) zero1_allgather_kernel(const __grid_constant__ AgParams<CAP> p)
+{
+    __shared__ __align__(128) AgSmem sm;
+    const int lane = threadIdx.x;
+    const uint64_t tile_elems = (uint64_t)(kAgBytes / p.esize);
+    const uint64_t item = blockIdx.x;
+    if (item == (uint64_t)p.world * p.tiles_per_shard) {          // the tails
+        if (lane == 0) {
+            for (int r = 0; r < p.world; ++r) {
+                uint64_t len, vlen;
+                shard_extent(p.n, p.shard_len, r, p.esize, len, vlen);
+                for (uint64_t i = vlen; i < len; ++i) {
+                    const uint64_t dst = ((uint64_t)r * p.shard_len + i) * p.esize;
+                    for (int q = 0; q < p.world; ++q) {
+                        if (p.esize == 2)
+                            *reinterpret_cast<uint16_t *>(p.out[q] + dst) =
+                                reinterpret_cast<const uint16_t *>(p.shards[r])[i];
+                        else
+                            *reinterpret_cast<uint32_t *>(p.out[q] + dst) =
+                                reinterpret_cast<const uint32_t *>(p.shards[r])[i];
+                    }
+                }
+            }
+        }
+        return;
+    }
+    const int r = (int)(item / p.tiles_per_shard);
+    const uint64_t e0 = (item % p.tiles_per_shard) * tile_elems;
+    uint64_t len, vlen;
+    shard_extent(p.n, p.shard_len, r, p.esize, len, vlen);
+    if (e0 >= vlen) return;                                       // past a short or empty shard
+    const uint32_t bytes = (uint32_t)((vlen - e0 < tile_elems ? vlen - e0 : tile_elems) * p.esize);
+    int abort_flag = 0;
+    volatile int *abort = &abort_flag;
+    unsigned *errors = p.errors;
+    unsigned local = 0;
+    if (!errors) errors = &local;
+    if (lane == 0) {
+        mbar_init(&sm.full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const uint64_t once = policy_evict_first();
+    if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.full, bytes);
+        tma_load_hint(sm.tile, p.shards[r] + e0 * p.esize, bytes, &sm.full, once);
+    }
+    const bool got = mbar_wait(&sm.full, 0, abort, errors);
+    if (!__all_sync(0xFFFFFFFFu, got)) {
+        // Let the load land (bounded) before the CTA's shared memory goes away.
+        if (lane == 0) drain_loads<1>(&sm.full, 1);
+        return;
+    }
+    const uint64_t dst = ((uint64_t)r * p.shard_len + e0) * p.esize;
+    for (int q = lane; q < p.world; q += 32) tma_store_hint(p.out[q] + dst, sm.tile, bytes, once);
+    tma_commit();
+    tma_wait_read<0>();
+}
+
+template <int CAP>
+cudaError_t launch_ag(uint64_t n, int world, uint64_t shard_len, int esize, const void *const *shards,
+                      void *const *out, unsigned *errors, cudaStream_t stream)
+{
+    AgParams<CAP> p{};
+    for (int r = 0; r < world; ++r) {
+        p.shards[r] = static_cast<const unsigned char *>(shards[r]);
+        p.out[r] = static_cast<unsigned char *>(out[r]);
+    }
+    const uint64_t tile_elems = kAgBytes / esize;
+    p.errors = errors;
+    p.n = n;
+    p.shard_len = shard_len;
+    p.tiles_per_shard = (shard_len + tile_elems - 1) / tile_elems;
+    p.world = world;
+    p.esize = esize;
+    const uint64_t grid = (uint64_t)world * p.tiles_per_shard + 1;
+    if (grid > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+    zero1_allgather_kernel<CAP><<<(unsigned)grid, 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 int afail(int code, const char *msg)
 {
     set_error_message(msg);
@@ -354,6 +474,38 @@ extern "C" int zero1_allreduce(uint64_t n, int world, int dtype, int op, const v
     e = dtype == ZERO1_DTYPE_BF16
             ? launch_ar_t<uint16_t>(n, world, op == ZERO1_OP_AVG, in_ptrs, out_ptrs, errors, sms, st)
             : launch_ar_t<float>(n, world, op == ZERO1_OP_AVG, in_ptrs, out_ptrs, errors, sms, st);
+    if (e != cudaSuccess) return afail(ZERO1_ECUDA, cudaGetErrorString(e));
+    return ZERO1_OK;
+}
+
+extern "C" int zero1_allgather(uint64_t n, int world, uint64_t shard_len, int dtype, const void *const *shard_ptrs,
+                               void *const *out_ptrs, unsigned *errors, void *stream)
+{
+    using namespace zero1;
+    if (n == 0) return afail(ZERO1_EINVAL, "zero1_allgather: n must be > 0");
+    if (world < 1 || world > ZERO1_MAX_WORLD) return afail(ZERO1_EINVAL, "zero1_allgather: bad world size");
+    if (dtype != ZERO1_DTYPE_BF16 && dtype != ZERO1_DTYPE_F32) return afail(ZERO1_EINVAL, "zero1_allgather: bad dtype");
+    if (shard_len == 0 || shard_len % 8 || shard_len > ((uint64_t)1 << 50) || shard_len * (uint64_t)world < n)
+        return afail(ZERO1_EINVAL, "zero1_allgather: shard_len must be a multiple of 8 with shard_len*world >= n");
+    if (!shard_ptrs || !out_ptrs) return afail(ZERO1_EINVAL, "zero1_allgather: pointer array is NULL");
+    for (int r = 0; r < world; ++r) {
+        const bool empty = (uint64_t)r * shard_len >= n;
+        if (!out_ptrs[r] || (!empty && !shard_ptrs[r]))
+            return afail(ZERO1_EINVAL, "zero1_allgather: a rank buffer is NULL");
+        if (!aligned16(out_ptrs[r]) || (!empty && !aligned16(shard_ptrs[r])))
+            return afail(ZERO1_EALIGN, "zero1_allgather: rank buffers must be 16-byte aligned");
+    }
+    if (errors && (reinterpret_cast<uintptr_t>(errors) & 3u))
+        return afail(ZERO1_EALIGN, "zero1_allgather: errors must be 4-byte aligned");
+    const int esize = dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (world <= 8)
+        e = launch_ag<8>(n, world, shard_len, esize, shard_ptrs, out_ptrs, errors, st);
+    else if (world <= 64)
+        e = launch_ag<64>(n, world, shard_len, esize, shard_ptrs, out_ptrs, errors, st);
+    else
+        e = launch_ag<512>(n, world, shard_len, esize, shard_ptrs, out_ptrs, errors, st);
     if (e != cudaSuccess) return afail(ZERO1_ECUDA, cudaGetErrorString(e));
     return ZERO1_OK;
 }
