@@ -184,6 +184,22 @@ int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const v
                         void *stream);
 int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream);
 
+/* The host-buffer step, pipelined: enqueue and return.  Uploads this step's
+ * gradients while the previous step's replicas are still downloading (the
+ * two directions of the host link run at once), through two alternating
+ * staging sets and separate upload and download copy streams.  Ordering:
+ * the step runs on `stream` after the previous step; a staging set is
+ * reused only after its last download finished.  The caller must keep
+ * host_grads unchanged and must not read host_params until
+ * zero1_host_sync(h) returns (host buffers may be the same every call).
+ * The first call allocates 8*W*n bytes of staging and creates the streams;
+ * zero1_destroy frees them.  Errors as zero1_step_host. */
+int zero1_step_host_async(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
+
+/* Wait for every host-path copy of the handle (and so for the steps they
+ * follow).  Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
+int zero1_host_sync(zero1_handle h);
+
 /* Checkpoint restore ("Parallel training", "training loop and checkpoint":
  * a checkpoint carries m, v and t).  master, m, v: arrays of n entries in
  * device or host memory (copied with cudaMemcpyDefault): master fp32, m and

@@ -300,6 +300,41 @@ def test_step_host_matches_device_step():
     assert all(bits_equal(a, b) for a, b in zip(sa[:3], sb[:3]))
 
 
+def test_step_host_async_matches_step_host():
+    """The pipelined host entry point gives the blocking one's results, step
+    by step: four steps with a fresh output buffer set per step (each read
+    after the final sync), then two with one shared set."""
+    w = WL.Workload("host_async", 100_003, 4, 0.01, 2, max_norm=0.05)
+    zhp, _ = _hp(w)
+    m0 = WL.master(w, "cuda")
+    steps = 6
+    hgs = [[x.cpu().pin_memory() for x in WL.grads(w, t, "cuda")] for t in range(1, steps + 1)]
+    fresh = lambda: [torch.empty(w.n, dtype=torch.bfloat16).pin_memory() for _ in range(w.world)]
+    want = []
+    with z.Zero1(w.n, w.world, zhp) as opt:
+        opt.set_state(m0)
+        for t in range(steps):
+            out = fresh()
+            opt.step_host(hgs[t], out)
+            want.append([u16(r) for r in out])
+        want_state = _state(opt, w.n)
+    with z.Zero1(w.n, w.world, zhp) as opt:
+        opt.set_state(m0)
+        outs = [fresh() for _ in range(4)]
+        for t in range(4):
+            opt.step_host_async(hgs[t], outs[t])
+        opt.host_sync()
+        for t in range(4):
+            assert all(np.array_equal(u16(a), b) for a, b in zip(outs[t], want[t])), t
+        shared = fresh()
+        for t in range(4, steps):
+            opt.step_host_async(hgs[t], shared)
+        opt.host_sync()
+        assert all(np.array_equal(u16(a), b) for a, b in zip(shared, want[steps - 1]))
+        got_state = _state(opt, w.n)
+    assert all(bits_equal(a, b) for a, b in zip(got_state[:3], want_state[:3]))
+
+
 # --------------------------------------------------------- full sizes
 
 def _windows(n: int, world: int, shard: int, rng, width=4096, n_random=8):

@@ -20,6 +20,7 @@ from dataclasses import dataclass
 __all__ = [
     "Zero1Error", "Hparams", "Options", "Zero1",
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
+    "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
     "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
@@ -40,6 +41,8 @@ _SIGS = {
     "zero1_destroy": (_I32, [_P]),
     "zero1_step": (_I32, [_P, _P, _P, _P]),
     "zero1_step_host": (_I32, [_P, _P, _P, _P]),
+    "zero1_step_host_async": (_I32, [_P, _P, _P, _P]),
+    "zero1_host_sync": (_I32, [_P]),
     "zero1_set_state": (_I32, [_P, _P, _P, _P, _U64, _P]),
     "zero1_get_state": (_I32, [_P, _P, _P, _P, _P, _P]),
     "zero1_set_state_range": (_I32, [_P, _U64, _U64, _P, _P, _P, _P]),
@@ -193,6 +196,15 @@ def zero1_step_host(h: int, host_grads, host_params, stream=None) -> None:
     _check(_load().zero1_step_host(h, _ptrs(host_grads), _ptrs(host_params), _stream(stream)))
 
 
+def zero1_step_host_async(h: int, host_grads, host_params, stream=None) -> None:
+    """Pipelined host-buffer step; host_params are valid after zero1_host_sync."""
+    _check(_load().zero1_step_host_async(h, _ptrs(host_grads), _ptrs(host_params), _stream(stream)))
+
+
+def zero1_host_sync(h: int) -> None:
+    _check(_load().zero1_host_sync(h))
+
+
 def zero1_set_state(h: int, master, m=None, v=None, t: int = 0, stream=None) -> None:
     _check(_load().zero1_set_state(h, _addr(master), _addr(m), _addr(v), t, _stream(stream)))
 
@@ -306,6 +318,12 @@ class Zero1:
 
     def step_host(self, grads, params, stream=None) -> None:
         zero1_step_host(self.handle, grads, params, stream)
+
+    def step_host_async(self, grads, params, stream=None) -> None:
+        zero1_step_host_async(self.handle, grads, params, stream)
+
+    def host_sync(self) -> None:
+        zero1_host_sync(self.handle)
 
     def set_state(self, master, m=None, v=None, t: int = 0, stream=None) -> None:
         zero1_set_state(self.handle, master, m, v, t, stream)

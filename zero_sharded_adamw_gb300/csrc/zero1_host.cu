@@ -27,6 +27,13 @@
 #include "zero1.h"
 #include "zero1_internal.h"
 
+// A set of copy streams that host<->device copies are dealt over.
+struct CopyLanes {
+    bool ready = false;
+    cudaStream_t s[4] = {};
+    cudaEvent_t fork = nullptr, join[4] = {};
+};
+
 struct zero1_ctx {
     uint64_t n = 0;
     int world = 0;
@@ -50,9 +57,14 @@ struct zero1_ctx {
     // copy streams its host<->device copies are spread over
     void *staging = nullptr;
     uint64_t staging_stride = 0;
-    bool copy_ready = false;
-    cudaStream_t copy_stream[4] = {};
-    cudaEvent_t copy_fork = nullptr, copy_join[4] = {};
+    CopyLanes copy;
+    // pipelined host path (zero1_step_host_async): two staging sets, upload
+    // and download lanes, and per set the events its last download recorded
+    void *astaging = nullptr;
+    int aset = 0;
+    bool aused[2] = {false, false};
+    CopyLanes up, down;
+    cudaEvent_t afree[2][4] = {};
     // per-kernel timing (zero1_profile_start/stop): 3 events per step
     std::vector<cudaEvent_t> prof;
     int prof_capacity = 0, prof_used = 0;
@@ -250,13 +262,18 @@ int zero1_destroy(zero1_handle h)
     if (h->bucket_sums) cudaFree(h->bucket_sums);
     if (h->ghat_bucket) cudaFree(h->ghat_bucket);
     for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
-    if (h->copy_ready) {
+    for (CopyLanes *l : {&h->copy, &h->up, &h->down}) {
+        if (!l->ready) continue;
         for (int i = 0; i < 4; ++i) {
-            cudaStreamDestroy(h->copy_stream[i]);
-            cudaEventDestroy(h->copy_join[i]);
+            cudaStreamDestroy(l->s[i]);
+            cudaEventDestroy(l->join[i]);
         }
-        cudaEventDestroy(h->copy_fork);
+        cudaEventDestroy(l->fork);
     }
+    for (auto &set : h->afree)
+        for (cudaEvent_t ev : set)
+            if (ev) cudaEventDestroy(ev);
+    if (h->astaging) cudaFree(h->astaging);
     delete h;
     if (e1 != cudaSuccess) return cuda_fail(e1, "cudaDeviceSynchronize in destroy");
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
@@ -311,39 +328,50 @@ constexpr uint64_t kCopyChunk = 64ull << 20;
 // round-robin over the handle's copy streams so that several copy engines
 // run at once; they start after the work already on `st` and the work
 // enqueued on `st` afterwards waits for all of them.
-int spread_copies(zero1_ctx *h, void *const *dst, const void *const *src, int count, uint64_t bytes,
-                  cudaMemcpyKind kind, cudaStream_t st)
+int lanes_ready(CopyLanes &l)
 {
+    if (l.ready) return ZERO1_OK;
     cudaError_t e;
-    if (!h->copy_ready) {
-        for (int i = 0; i < kCopyStreams; ++i) {
-            if ((e = cudaStreamCreateWithFlags(&h->copy_stream[i], cudaStreamNonBlocking)) != cudaSuccess)
-                return cuda_fail(e, "cudaStreamCreate");
-            if ((e = cudaEventCreateWithFlags(&h->copy_join[i], cudaEventDisableTiming)) != cudaSuccess)
-                return cuda_fail(e, "cudaEventCreate");
-        }
-        if ((e = cudaEventCreateWithFlags(&h->copy_fork, cudaEventDisableTiming)) != cudaSuccess)
+    for (int i = 0; i < kCopyStreams; ++i) {
+        if ((e = cudaStreamCreateWithFlags(&l.s[i], cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreate");
+        if ((e = cudaEventCreateWithFlags(&l.join[i], cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "cudaEventCreate");
-        h->copy_ready = true;
     }
-    if ((e = cudaEventRecord(h->copy_fork, st)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreate");
+    l.ready = true;
+    return ZERO1_OK;
+}
+
+// `count` copies of `bytes` each, cut into chunks of at most 64 MiB and dealt
+// round-robin over the lanes so that several copy engines run at once; they
+// start after the work already on `st`.  With join_back, the work enqueued
+// on `st` afterwards waits for all of them; either way l.join[i] marks the
+// end of lane i's part.
+int spread_copies(CopyLanes &l, void *const *dst, const void *const *src, int count, uint64_t bytes,
+                  cudaMemcpyKind kind, cudaStream_t st, bool join_back)
+{
+    int rc = lanes_ready(l);
+    if (rc) return rc;
+    cudaError_t e;
+    if ((e = cudaEventRecord(l.fork, st)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     for (int i = 0; i < kCopyStreams; ++i)
-        if ((e = cudaStreamWaitEvent(h->copy_stream[i], h->copy_fork, 0)) != cudaSuccess)
+        if ((e = cudaStreamWaitEvent(l.s[i], l.fork, 0)) != cudaSuccess)
             return cuda_fail(e, "cudaStreamWaitEvent");
     int next = 0;
     for (int r = 0; r < count; ++r) {
         for (uint64_t off = 0; off < bytes; off += kCopyChunk) {
             const uint64_t len = bytes - off < kCopyChunk ? bytes - off : kCopyChunk;
             e = cudaMemcpyAsync(static_cast<char *>(dst[r]) + off, static_cast<const char *>(src[r]) + off, len,
-                                kind, h->copy_stream[next]);
+                                kind, l.s[next]);
             if (e != cudaSuccess) return cuda_fail(e, "host/device copy");
             next = (next + 1) % kCopyStreams;
         }
     }
     for (int i = 0; i < kCopyStreams; ++i) {
-        if ((e = cudaEventRecord(h->copy_join[i], h->copy_stream[i])) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-        if ((e = cudaStreamWaitEvent(st, h->copy_join[i], 0)) != cudaSuccess)
+        if ((e = cudaEventRecord(l.join[i], l.s[i])) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if (join_back && (e = cudaStreamWaitEvent(st, l.join[i], 0)) != cudaSuccess)
             return cuda_fail(e, "cudaStreamWaitEvent");
     }
     return ZERO1_OK;
@@ -375,13 +403,77 @@ int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *
         dg[r] = base + (uint64_t)r * h->staging_stride;
         dp[r] = base + (uint64_t)(h->world + r) * h->staging_stride;
     }
-    int rc = spread_copies(h, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st);
+    int rc = spread_copies(h->copy, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st, true);
     if (rc) return rc;
     rc = zero1_step(h, dg, dp, stream);
     if (rc) return rc;
-    rc = spread_copies(h, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st);
+    rc = spread_copies(h->copy, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st, true);
     if (rc) return rc;
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return ZERO1_OK;
+}
+
+int zero1_step_host_async(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!host_grads || !host_params) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r)
+        if (!host_grads[r] || !host_params[r]) return fail(ZERO1_EINVAL, "rank %d host buffer is NULL", r);
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t bytes = h->n * 2;
+    const uint64_t stride = round_up(bytes, 256);
+    cudaError_t e;
+    if (!h->astaging) {
+        if ((e = cudaMalloc(&h->astaging, 4 * (uint64_t)h->world * stride)) != cudaSuccess) {
+            h->astaging = nullptr;
+            return cuda_fail(e, "cudaMalloc of staging buffers");
+        }
+        for (auto &set : h->afree)
+            for (cudaEvent_t &ev : set)
+                if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+                    return cuda_fail(e, "cudaEventCreate");
+    }
+    int rc;
+    if ((rc = lanes_ready(h->up)) || (rc = lanes_ready(h->down))) return rc;
+    const int set = h->aset;
+    void *dg[ZERO1_MAX_WORLD];
+    void *dp[ZERO1_MAX_WORLD];
+    char *base = static_cast<char *>(h->astaging) + (uint64_t)set * 2 * h->world * stride;
+    for (int r = 0; r < h->world; ++r) {
+        dg[r] = base + (uint64_t)r * stride;
+        dp[r] = base + (uint64_t)(h->world + r) * stride;
+    }
+    // This staging set is free once the download that last read it is done.
+    if (h->aused[set]) {
+        for (int i = 0; i < kCopyStreams; ++i) {
+            if ((e = cudaStreamWaitEvent(st, h->afree[set][i], 0)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamWaitEvent");
+        }
+    }
+    if ((rc = spread_copies(h->up, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st, true))) return rc;
+    if ((rc = zero1_step(h, dg, dp, stream))) return rc;
+    if ((rc = spread_copies(h->down, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st, false)))
+        return rc;
+    for (int i = 0; i < kCopyStreams; ++i)
+        if ((e = cudaEventRecord(h->afree[set][i], h->down.s[i])) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+    h->aused[set] = true;
+    h->aset = 1 - set;
+    return ZERO1_OK;
+}
+
+int zero1_host_sync(zero1_handle h)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    DeviceGuard g(h->device);
+    for (CopyLanes *l : {&h->up, &h->down, &h->copy}) {
+        if (!l->ready) continue;
+        for (int i = 0; i < kCopyStreams; ++i) {
+            cudaError_t e = cudaStreamSynchronize(l->s[i]);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        }
+    }
     return ZERO1_OK;
 }
 

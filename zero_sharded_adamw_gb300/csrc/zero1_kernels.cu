@@ -47,7 +47,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kTile = 2048;                      // parameters per tile
-constexpr int kStages = 4;                       // shared-memory ring depth
+constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel
+constexpr int kUpdStages = 4;                    // shared-memory ring depth, update kernel
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
@@ -391,10 +392,10 @@ __device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, 
 }
 
 struct UpdSmem {
-    float in[kStages][4][kTile];   // 128 KB: ghat (or the W <= 2 bf16 grads), master, m, v
+    float in[kUpdStages][4][kTile];   // 32 KB per stage: ghat (or the W <= 2 bf16 grads), master, m, v
                                    // (m, v use half their slot when stored in bf16)
-    uint16_t b16[kStages][kTile];  // 16 KB: the tile's bf16 parameters
-    uint64_t full[kStages], done[kStages], empty[kStages];
+    uint16_t b16[kUpdStages][kTile];  // 4 KB per stage: the tile's bf16 parameters
+    uint64_t full[kUpdStages], done[kUpdStages], empty[kUpdStages];
     int abort;
     float clip;
 };
@@ -478,7 +479,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     volatile int *abort = &sm.abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kUpdStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.done[s], kConsumerWarps);
             mbar_init(&sm.empty[s], 1);
@@ -507,8 +508,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         if (lane == 0) {
             uint32_t k = 0;
             for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
-                const int s = k % kStages;
-                if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
+                const int s = k % kUpdStages;
+                if (k >= kUpdStages && !mbar_wait(&sm.empty[s], ((k / kUpdStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
                 const uint64_t base = (uint64_t)j * kTile;
                 const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
                 const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
@@ -526,7 +527,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
                 tma_load_hint(sm.in[s][3], static_cast<const unsigned char *>(p.v) + base * kMomBytes,
                               cnt * kMomBytes, &sm.full[s], once);
             }
-            if (*abort) drain_loads<kStages>(sm.full, k);
+            if (*abort) drain_loads<kUpdStages>(sm.full, k);
         }
         return;
     }
@@ -534,8 +535,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     if (warp == kConsumerWarps + 1) {                             // stores
         uint32_t k = 0;
         for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
-            const int s = k % kStages;
-            const bool got = mbar_wait(&sm.done[s], (k / kStages) & 1u, abort, &p.status->errors);
+            const int s = k % kUpdStages;
+            const bool got = mbar_wait(&sm.done[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             const uint64_t base = (uint64_t)j * kTile;
             const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
@@ -555,7 +556,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             if (k >= 1) {                      // the previous tile's stores have read its stage
                 tma_wait_read<1>();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.empty[(k - 1) % kStages]);
+                if (lane == 0) mbar_arrive(&sm.empty[(k - 1) % kUpdStages]);
             }
         }
         tma_wait_all();
@@ -569,8 +570,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     const uint32_t o0 = threadIdx.x * 4u, o1 = kTile / 2 + threadIdx.x * 4u;
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
-        const int s = k % kStages;
-        const bool got = mbar_wait(&sm.full[s], (k / kStages) & 1u, abort, &p.status->errors);
+        const int s = k % kUpdStages;
+        const bool got = mbar_wait(&sm.full[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint64_t base = (uint64_t)j * kTile;
         const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
