@@ -78,26 +78,38 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch of the update kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"zero1_adamw_ag_kernel_{workload.replace('@', '_n')}.txt")
-    if not os.path.exists(path):
-        return None
-    with open(KERNEL_SRC, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+def _summary_fields(path: str) -> dict:
     fields = {}
     with open(path) as f:
         for line in f:
             if ":" in line:
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("kernel_source_sha256") != sha:
-        return None
-    try:
-        return float(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return fields
+
+
+def kernel_traffic(workload: str) -> tuple[float | None, str | None]:
+    """DRAM bytes per launch of the update kernel from a committed ncu
+    summary taken on the current kernel source, and that summary's name:
+    the full-size one-pass capture of the workload if there is one, else a
+    small-case capture scaled to the workload's size.  (None, None) when
+    neither matches the current source."""
+    with open(KERNEL_SRC, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    name = workload.replace("@", "_n")
+    for fname, key in ((f"dram_{name}.txt", "zero1_adamw_ag_kernel.dram_bytes_per_launch"),
+                       (f"zero1_adamw_ag_kernel_{name}.txt", "dram_bytes_per_launch")):
+        path = os.path.join(ROOT, "profiles", fname)
+        if not os.path.exists(path):
+            continue
+        fields = _summary_fields(path)
+        if fields.get("kernel_source_sha256") != sha:
+            continue
+        try:
+            return float(fields[key]), "profiles/" + fname
+        except (KeyError, ValueError):
+            continue
+    return None, None
 
 
 class ClockSampler:
@@ -222,9 +234,15 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     opt.set_state(WL.master(w, dev), stream=stream)
     torch.cuda.synchronize(dev)
 
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup):
+        if i == 0:
+            w0.record(stream)
         opt.step(grad_sets[i % 2], reps, stream)
+        if i == 0:
+            w1.record(stream)
     torch.cuda.synchronize(dev)
+    first_ms = w0.elapsed_time(w1) if args.warmup else None
 
     clocks = ClockSampler(local_rank)
     time.sleep(0.3 if clocks.proc else 0.0)
@@ -241,6 +259,8 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     barrier(world_size)
     t1 = time.time()
     local_ms = ev0.elapsed_time(ev1)
+    per_rs, per_upd = z.zero1_profile_read(opt.handle, args.steps)
+    per_step = sorted(x + y for x, y in zip(per_rs, per_upd))
     rs_ms, upd_ms, prof_steps = z.zero1_profile_stop(opt.handle)
     clk = clocks.stop(t0, t1)
     ms = reduce_max(local_ms, world_size, dev)
@@ -255,7 +275,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     rs_avg = rs_ms / max(1, prof_steps)
     upd_bytes = (state_rw + 2 * w.world) * w.n    # state read+write, replica writes
     rs_bytes = (2 * w.world) * w.n                # gradient reads
-    traffic = kernel_traffic(w.name)
+    traffic, traffic_src = kernel_traffic(w.name)
     achieved = upd_bytes / (upd_avg / 1e3) / 1e9
 
     # End to end through the host-buffer entry points: every step uploads
@@ -305,7 +325,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
                 "frac_of_peak": (alg_step / (ms_per_step / 1e3) / 1e9) / peak,
                 "peak_gbs": peak, "peak_kind": peak_kind},
         "roofline": {"bound": "hbm", "kernel": "zero1_adamw_ag_kernel", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes_per_launch": upd_bytes, "avg_launch_ms": upd_avg,
                      "peak_kind": peak_kind},
         "kernels": {
@@ -314,6 +334,11 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
             "zero1_adamw_ag_kernel": {"avg_launch_ms": upd_avg, "algorithmic_bytes": upd_bytes,
                                       "gbs": achieved},
             "launches_timed": prof_steps},
+        # per-step K1 + K2 device time from the same events (gaps between
+        # steps excluded), and the first warm-up step on its own
+        "step_kernel_ms": {"median": per_step[len(per_step) // 2] if per_step else None,
+                           "min": per_step[0] if per_step else None,
+                           "first_warmup_step": first_ms},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": 2 * args.steps,
         "last_step": {"grad_norm": norm, "clip_coef": clip},

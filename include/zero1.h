@@ -254,6 +254,14 @@ int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint
 int zero1_profile_start(zero1_handle h, int capacity);
 int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, uint64_t *steps);
 
+/* The per-step kernel times recorded so far, before zero1_profile_stop:
+ * waits for the last recorded event, then writes step i's reduce-scatter +
+ * norm and update + all-gather durations (ms) to rs_norm_ms[i] and
+ * update_ms[i] for i < min(recorded, capacity) and the number recorded to
+ * *steps.  Arrays are caller-owned host memory and may be NULL.  The events
+ * stay alive.  Errors: ZERO1_EINVAL (no profiling started), ZERO1_ECUDA. */
+int zero1_profile_read(zero1_handle h, float *rs_norm_ms, float *update_ms, uint64_t capacity, uint64_t *steps);
+
 /* Host-only planning (no device needed).  The shard length S = ceil(n/W)
  * rounded up to 64 and the padded state length W*S for n parameters over
  * `world` ranks.  Errors: ZERO1_EINVAL (n == 0 or world out of range). */

@@ -275,6 +275,30 @@ def test_layout_and_footprint():
             assert state + scratch <= nbytes <= state + scratch + 64 * 1024
 
 
+def test_profile_events():
+    """zero1_profile_read returns one positive (K1, K2) pair per profiled
+    step, agreeing with zero1_profile_stop's sums; steps past the capacity
+    are not recorded."""
+    w = WL.Workload("prof", 1_000_003, 8, 0.001, 1)
+    zhp, _ = _hp(w)
+    g = WL.grads(w, 1, "cuda")
+    reps = [torch.empty_like(g[0]) for _ in range(w.world)]
+    with z.Zero1(w.n, w.world, zhp) as opt:
+        opt.set_state(WL.master(w, "cuda"))
+        z.zero1_profile_start(opt.handle, 3)
+        for _ in range(5):
+            opt.step(g, reps)
+        rs, upd = z.zero1_profile_read(opt.handle, 8)
+        assert len(rs) == len(upd) == 3
+        assert all(x > 0 for x in rs + upd)
+        assert z.zero1_profile_read(opt.handle, 2)[0] == rs[:2]
+        a, b, k = z.zero1_profile_stop(opt.handle)
+        assert k == 3
+        assert math.isclose(a, sum(rs), rel_tol=1e-5) and math.isclose(b, sum(upd), rel_tol=1e-5)
+        with pytest.raises(z.Zero1Error):
+            z.zero1_profile_read(opt.handle, 1)
+
+
 def test_step_host_matches_device_step():
     """The host-buffer entry point equals the device entry point."""
     w = WL.Workload("host", 100_003, 4, 0.01, 2, max_norm=0.05)

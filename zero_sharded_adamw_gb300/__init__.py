@@ -23,7 +23,7 @@ __all__ = [
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -55,6 +55,7 @@ _SIGS = {
     "zero1_bucket_finish": (_I32, [_P, _P, _P]),
     "zero1_profile_start": (_I32, [_P, _I32]),
     "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
+    "zero1_profile_read": (_I32, [_P, _P, _P, _U64, _P]),
     "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
@@ -262,6 +263,14 @@ def zero1_profile_stop(h: int) -> tuple[float, float, int]:
     a, b, n = C.c_double(), C.c_double(), C.c_uint64()
     _check(_load().zero1_profile_stop(h, C.byref(a), C.byref(b), C.byref(n)))
     return a.value, b.value, n.value
+
+
+def zero1_profile_read(h: int, capacity: int) -> tuple[list[float], list[float]]:
+    """Per-step (reduce-scatter+norm ms, update+all-gather ms) recorded so far."""
+    a, b, n = (C.c_float * max(1, capacity))(), (C.c_float * max(1, capacity))(), C.c_uint64()
+    _check(_load().zero1_profile_read(h, a, b, capacity, C.byref(n)))
+    k = min(n.value, capacity)
+    return list(a[:k]), list(b[:k])
 
 
 def zero1_shard_plan(n: int, world: int) -> tuple[int, int]:

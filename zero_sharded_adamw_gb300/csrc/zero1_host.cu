@@ -616,6 +616,27 @@ int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, ui
     return ZERO1_OK;
 }
 
+int zero1_profile_read(zero1_handle h, float *rs_norm_ms, float *update_ms, uint64_t capacity, uint64_t *steps)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (h->prof_capacity == 0) return fail(ZERO1_EINVAL, "profiling was not started");
+    DeviceGuard g(h->device);
+    cudaError_t e = cudaSuccess;
+    if (h->prof_used > 0) e = cudaEventSynchronize(h->prof[3 * (size_t)h->prof_used - 1]);
+    const uint64_t used = (uint64_t)h->prof_used;
+    const uint64_t k = used < capacity ? used : capacity;
+    for (uint64_t i = 0; e == cudaSuccess && i < k; ++i) {
+        float x = 0.f, y = 0.f;
+        e = cudaEventElapsedTime(&x, h->prof[3 * i], h->prof[3 * i + 1]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&y, h->prof[3 * i + 1], h->prof[3 * i + 2]);
+        if (rs_norm_ms) rs_norm_ms[i] = x;
+        if (update_ms) update_ms[i] = y;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "event timing");
+    if (steps) *steps = used;
+    return ZERO1_OK;
+}
+
 int zero1_bucket_begin(zero1_handle h)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
