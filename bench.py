@@ -227,13 +227,16 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     stream = torch.cuda.current_stream(dev)
 
     hp = z.Hparams(**w.hparams())
-    opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16)
+    opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step)
     grad_sets = [WL.grads(w, t, dev) for t in (1, 2)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     opt = z.Zero1(w.n, w.world, hp, opts)
     opt.set_state(WL.master(w, dev), stream=stream)
     torch.cuda.synchronize(dev)
 
+    # pointer tables built once: the timed loop marshals no per-step arguments
+    tables = [z.PtrTable(g) for g in grad_sets]
+    rep_table = z.PtrTable(reps)
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup):
         if i == 0:
@@ -252,8 +255,10 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     t0 = time.time()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    h0 = time.perf_counter()
     for i in range(args.steps):
-        opt.step(grad_sets[i % 2], reps, stream)
+        opt.step(tables[i % 2], rep_table, stream)
+    host_enqueue_s = time.perf_counter() - h0
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world_size)
@@ -277,6 +282,22 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     rs_bytes = (2 * w.world) * w.n                # gradient reads
     traffic, traffic_src = kernel_traffic(w.name)
     achieved = upd_bytes / (upd_avg / 1e3) / 1e9
+    launches = opt.launches_per_step()
+    if launches == 1:
+        # one-launch small-n path: the step's one kernel moves every byte
+        achieved = alg_step / (rs_avg / 1e3) / 1e9
+        kernels = {"zero1_small_step_kernel": {"avg_launch_ms": rs_avg, "algorithmic_bytes": alg_step,
+                                               "gbs": achieved},
+                   "launches_timed": prof_steps}
+        roof_kernel, roof_bytes, roof_ms = "zero1_small_step_kernel", alg_step, rs_avg
+        traffic, traffic_src = None, None
+    else:
+        kernels = {"zero1_rs_norm_kernel": {"avg_launch_ms": rs_avg, "algorithmic_bytes": rs_bytes,
+                                            "gbs": rs_bytes / (rs_avg / 1e3) / 1e9},
+                   "zero1_adamw_ag_kernel": {"avg_launch_ms": upd_avg, "algorithmic_bytes": upd_bytes,
+                                             "gbs": achieved},
+                   "launches_timed": prof_steps}
+        roof_kernel, roof_bytes, roof_ms = "zero1_adamw_ag_kernel", upd_bytes, upd_avg
 
     # End to end through the host-buffer entry points: every step uploads
     # every rank's gradient from pinned memory, runs the step and downloads
@@ -324,23 +345,21 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
                 "algorithmic_gbs": world_size * alg_step / (ms_per_step / 1e3) / 1e9,
                 "frac_of_peak": (alg_step / (ms_per_step / 1e3) / 1e9) / peak,
                 "peak_gbs": peak, "peak_kind": peak_kind},
-        "roofline": {"bound": "hbm", "kernel": "zero1_adamw_ag_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
-                     "algorithmic_bytes_per_launch": upd_bytes, "avg_launch_ms": upd_avg,
+                     "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_ms": roof_ms,
                      "peak_kind": peak_kind},
-        "kernels": {
-            "zero1_rs_norm_kernel": {"avg_launch_ms": rs_avg, "algorithmic_bytes": rs_bytes,
-                                     "gbs": rs_bytes / (rs_avg / 1e3) / 1e9},
-            "zero1_adamw_ag_kernel": {"avg_launch_ms": upd_avg, "algorithmic_bytes": upd_bytes,
-                                      "gbs": achieved},
-            "launches_timed": prof_steps},
+        "kernels": kernels,
         # per-step K1 + K2 device time from the same events (gaps between
         # steps excluded), and the first warm-up step on its own
         "step_kernel_ms": {"median": per_step[len(per_step) // 2] if per_step else None,
                            "min": per_step[0] if per_step else None,
-                           "first_warmup_step": first_ms},
+                           "first_warmup_step": first_ms,
+                           # host time to enqueue one step (binding + C ABI + launches + profile
+                           # events); when it reaches ms_per_step the GPU waits on the host
+                           "host_enqueue_per_step": 1e3 * host_enqueue_s / args.steps},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches * args.steps,
         "last_step": {"grad_norm": norm, "clip_coef": clip},
     }
     opt.close()
@@ -642,6 +661,8 @@ def main(argv=None):
     ap.add_argument("--decay-first", action="store_true", help="variant: torch.optim.AdamW's decay order")
     ap.add_argument("--clip-eps", type=float, default=0.0, help="variant: clip eps (torch uses 1e-6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small-step", type=int, default=0, choices=[-1, 0, 1],
+                    help="one-launch small-n path: 0 automatic, 1 whenever n fits, -1 never")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -651,7 +672,7 @@ def main(argv=None):
     cfg = {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
            "bytes_per_param": 4 * w.world + (16 if args.moments_bf16 else 24), "hparams": w.hparams(),
            "variant": {"moments_bf16": args.moments_bf16, "decay_first": args.decay_first,
-                       "clip_eps": args.clip_eps},
+                       "clip_eps": args.clip_eps, "small_step": args.small_step},
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
                  else "working set fits in L2 (launch-latency bound)"}

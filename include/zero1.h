@@ -110,6 +110,11 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     d = bf16(bf16(sqrt(v)) + eps); the fp32 master update uses those.
  *   bucket_ctas: CTAs of each zero1_bucket_reduce launch (0 = one per SM).
  *     Fewer leave SMs to a backward running alongside on another stream.
+ *   small_step: the one-launch path for small n (a single thread-block
+ *     cluster runs the whole step; n <= 65,536): 0 = automatic (taken when
+ *     n <= 32,768 and (4W+24)*n <= 6 MiB), 1 = whenever n <= 65,536,
+ *     -1 = never.  Either path computes the same update; only the order of
+ *     the norm's partial sums differs (see zero1_get_grad_norm).
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -117,6 +122,7 @@ typedef struct zero1_options {
     double clip_eps;
     int32_t moments_bf16;
     int32_t bucket_ctas;
+    int32_t small_step;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).
@@ -138,8 +144,9 @@ int zero1_destroy(zero1_handle h);
  * The pointer arrays themselves are copied into the launch; the buffers must
  * stay valid until the stream reaches the step.  Gradient and replica
  * buffers must not overlap each other or the library's state.
- * Launches exactly two kernels: the reduce-scatter + norm kernel and the
- * clip + AdamW + bf16 + all-gather kernel.
+ * Launches two kernels, the reduce-scatter + norm kernel and the clip +
+ * AdamW + bf16 + all-gather kernel, or, for small n (zero1_options
+ * small_step), one kernel that does all of it (zero1_step_launches).
  * Errors: ZERO1_EINVAL (NULL handle / array / entry), ZERO1_EALIGN,
  * ZERO1_ECUDA (launch failure; t is then left unchanged). */
 int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_ptrs, void *stream);
@@ -253,6 +260,10 @@ int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint
  * Errors: ZERO1_EINVAL (capacity < 1, or stop without start), ZERO1_ECUDA. */
 int zero1_profile_start(zero1_handle h, int capacity);
 int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, uint64_t *steps);
+
+/* Kernel launches one zero1_step makes with this handle: 2, or 1 on the
+ * one-launch small-n path.  Errors: ZERO1_EINVAL. */
+int zero1_step_launches(zero1_handle h, int *launches);
 
 /* The per-step kernel times recorded so far, before zero1_profile_stop:
  * waits for the last recorded event, then writes step i's reduce-scatter +

@@ -45,7 +45,7 @@ def _state(opt: z.Zero1, n: int):
     return f32(master), f32(m), f32(v), t
 
 
-def run_parity(w: WL.Workload, steps: int, *, lr_schedule=None, master0=None):
+def run_parity(w: WL.Workload, steps: int, *, lr_schedule=None, master0=None, opts=None, launches=None):
     """Run `steps` steps of workload `w` on the GPU and both oracles; assert
     the protocol above at every step.  Returns the final GPU state."""
     zhp, ohp = _hp(w)
@@ -53,7 +53,9 @@ def run_parity(w: WL.Workload, steps: int, *, lr_schedule=None, master0=None):
     m0 = WL.master(w, "cuda") if master0 is None else master0
     grads = [Guarded(n, torch.bfloat16) for _ in range(w.world)]
     reps = [Guarded(n, torch.bfloat16) for _ in range(w.world)]
-    with z.Zero1(n, w.world, zhp) as opt:
+    with z.Zero1(n, w.world, zhp, opts) as opt:
+        if launches is not None:
+            assert opt.launches_per_step() == launches
         opt.set_state(m0, None, None, 0)
         inj, free = o.State(f32(m0)), o.State(f32(m0))
         for t in range(1, steps + 1):
@@ -95,12 +97,38 @@ def test_tiny_ten_steps():
     run_parity(WL.WORKLOADS["tiny"], 10)
 
 
+@pytest.mark.parametrize("path", ["one_launch", "two_kernels"])
 @pytest.mark.parametrize("world", [1, 2, 3, 4, 5, 8, 16, 64])
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 63, 65, 4097, 256 * 8 * 3 + 5])
-def test_shapes(n, world):
-    """Ragged and tiny sizes, every kernel specialisation, clip active."""
+def test_shapes(n, world, path):
+    """Ragged and tiny sizes, every kernel specialisation, clip active, on
+    the one-launch cluster path and on the two-kernel path."""
     w = WL.Workload(f"shape_{n}_{world}", n, world, 0.05, 3, max_norm=0.01)
-    run_parity(w, 3)
+    small = 1 if path == "one_launch" else -1
+    run_parity(w, 3, opts=z.Options(small_step=small), launches=1 if small == 1 else 2)
+
+
+@pytest.mark.parametrize("n", [16_383, 16_384, 16_391, 32_768, 32_775, 65_535, 65_536])
+def test_one_launch_vector_counts(n):
+    """The one-launch path at the edges of 1, 2 and 4 vectors per thread
+    (16,384 / 32,768 / 65,536 parameters), ragged tails included."""
+    w = WL.Workload(f"small_{n}", n, 8, 0.05, 2, max_norm=0.01)
+    run_parity(w, 2, opts=z.Options(small_step=1), launches=1)
+
+
+def test_one_launch_selection():
+    """Automatic choice: one launch while n <= 32,768 and (4W+24)*n <= 6 MiB;
+    a forced one-launch handle past 65,536 parameters keeps two kernels."""
+    for n, world, want in ((4096, 4, 1), (32_768, 8, 1), (16_384, 64, 1), (32_768, 64, 2), (32_769, 1, 2),
+                           (65_536, 8, 2), (1_000_000, 8, 2)):
+        with z.Zero1(n, world) as opt:
+            assert opt.launches_per_step() == want, (n, world)
+    with z.Zero1(65_537, 2, None, z.Options(small_step=1)) as opt:
+        assert opt.launches_per_step() == 2
+    with z.Zero1(16, 2, None, z.Options(small_step=-1)) as opt:
+        assert opt.launches_per_step() == 2
+    with pytest.raises(z.Zero1Error):
+        z.Zero1(16, 2, None, z.Options(small_step=2))
 
 
 def test_multi_tile_ragged_clip_on_and_off():

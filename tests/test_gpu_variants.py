@@ -4,9 +4,13 @@ order, a clip eps, m and v stored in bf16, and all three together.
 Same protocol as test_gpu_parity: with the GPU's clip coefficient injected
 the oracle's master, m, v and replicas must match bit for bit; the norm and
 the coefficient within 1e-6 of the oracle's own; the free-running oracle
-within 1e-6 relative (fp32 moments), or within one bf16 ulp on m and v and
-1e-3 relative on the master (bf16 moments, where a one-ulp difference in c
-can flip a moment's last bit).
+within 1e-6 relative (fp32 moments).  With bf16 moments a one-fp32-ulp
+difference in c can flip a bf16 rounding of m or v (and so of d) at any
+step, and the flips carry into later steps, so the free-running bounds are
+counted in bf16 roundings: after t steps m and v lie within t * 2^-6 of the
+oracle's at the array's RMS scale (each moment update rounds twice, and one
+bf16 ulp is at most 2^-7 relative), and the master within 2^-5 times the
+summed step sizes (two flipped roundings of |u| <= ~1 per step).
 """
 from __future__ import annotations
 
@@ -19,7 +23,7 @@ import torch
 import workloads as WL
 import zero_sharded_adamw_gb300 as z
 from oracle import zero1_oracle as o
-from tests.gpu_util import Guarded, bf16_ulp, bits_equal, f32, rel_err, u16
+from tests.gpu_util import Guarded, bits_equal, f32, rel_err, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -34,9 +38,14 @@ def _moments(opt: z.Zero1, n: int, bf16: bool):
     return f32(master), conv(m), conv(v)
 
 
-def run_variant(w: WL.Workload, steps: int, opts: o.Options):
+def _widen(x: np.ndarray) -> np.ndarray:
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+def run_variant(w: WL.Workload, steps: int, opts: o.Options, small_step: int = 0):
     d = w.hparams()
-    zopts = z.Options(opts.decay_before_update, opts.clip_eps, opts.moments_bf16)
+    step_budget = 0.0
+    zopts = z.Options(opts.decay_before_update, opts.clip_eps, opts.moments_bf16, small_step=small_step)
     ohp = o.HP(**d)
     m0 = WL.master(w, "cuda")
     grads = [Guarded(w.n, torch.bfloat16) for _ in range(w.world)]
@@ -61,8 +70,10 @@ def run_variant(w: WL.Workload, steps: int, opts: o.Options):
                 assert abs(norm_g - norm_i) <= 1e-6 * norm_i
                 assert abs(float(c_g) - float(c_f)) <= 1e-6 * float(c_f)
             if opts.moments_bf16:
-                assert bf16_ulp(m, free.m) <= 1 and bf16_ulp(v, free.v) <= 1
-                assert rel_err(master, free.master) <= 1e-3
+                step_budget += d["lr"] * math.sqrt(1 - d["beta2"] ** t) / (1 - d["beta1"] ** t)
+                assert rel_err(_widen(m), _widen(free.m)) <= t * 2.0 ** -6
+                assert rel_err(_widen(v), _widen(free.v)) <= t * 2.0 ** -6
+                assert float(np.max(np.abs(master.astype(np.float64) - free.master))) <= step_budget * 2.0 ** -5
             else:
                 assert rel_err(master, free.master) <= 1e-6
                 assert rel_err(m, free.m) <= 1e-6 and rel_err(v, free.v) <= 1e-6
@@ -81,6 +92,18 @@ def test_clip_eps():
 @pytest.mark.parametrize("n,world", [(1_000_003, 8), (65_541, 2), (7, 3), (4096, 1)])
 def test_bf16_moments(n, world):
     run_variant(WL.Workload("mv", n, world, 0.01, 5, max_norm=0.05), 5, o.Options(moments_bf16=True))
+
+
+@pytest.mark.parametrize("small_step", [1, -1])
+@pytest.mark.parametrize("variant", ["decay_first", "clip_eps", "bf16_moments", "all"])
+def test_variants_on_both_paths(variant, small_step):
+    """Each variant at a small ragged size on the one-launch cluster path
+    (small_step 1) and on the two-kernel path (-1)."""
+    opts = {"decay_first": o.Options(decay_before_update=True), "clip_eps": o.Options(clip_eps=1e-6),
+            "bf16_moments": o.Options(moments_bf16=True),
+            "all": o.Options(decay_before_update=True, clip_eps=1e-6, moments_bf16=True)}[variant]
+    w = WL.Workload("vp", 20_005, 3, 0.01, 4, lr=1e-2, weight_decay=0.5, max_norm=0.05)
+    run_variant(w, 4, opts, small_step)
 
 
 def test_all_variants_w64():

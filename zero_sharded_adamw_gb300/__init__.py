@@ -18,12 +18,12 @@ import os
 from dataclasses import dataclass
 
 __all__ = [
-    "Zero1Error", "Hparams", "Options", "Zero1",
+    "Zero1Error", "Hparams", "Options", "Zero1", "PtrTable",
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -56,6 +56,7 @@ _SIGS = {
     "zero1_profile_start": (_I32, [_P, _I32]),
     "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
     "zero1_profile_read": (_I32, [_P, _P, _P, _U64, _P]),
+    "zero1_step_launches": (_I32, [_P, _P]),
     "zero1_shard_plan": (_I32, [_U64, _I32, _P, _P]),
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
@@ -92,21 +93,23 @@ class Hparams:
 
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
-                ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32)]
+                ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32)]
 
 
 @dataclass
 class Options:
     """Step variants: torch.optim.AdamW's decay order, a clip eps (torch's
-    clip_grad_norm_ uses 1e-6), m and v stored in bf16."""
+    clip_grad_norm_ uses 1e-6), m and v stored in bf16; the bucketed step's
+    CTAs per bucket; the one-launch small-n path (0 auto, 1 on, -1 off)."""
     decay_before_update: bool = False
     clip_eps: float = 0.0
     moments_bf16: bool = False
     bucket_ctas: int = 0
+    small_step: int = 0
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
-                         1 if self.moments_bf16 else 0, self.bucket_ctas)
+                         1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step)
 
 
 _lib = None
@@ -156,7 +159,22 @@ def _stream(s) -> int | None:
     return int(s.cuda_stream) or None
 
 
+class PtrTable:
+    """A pointer array built once (W buffers' addresses), for callers that
+    pass the same buffers every step: it skips the per-call marshalling.
+    It keeps references to the buffers so that they outlive the table."""
+
+    def __init__(self, xs):
+        self.buffers = list(xs)
+        self.array = (C.c_void_p * len(self.buffers))(*[_addr(x) for x in self.buffers])
+
+    def __len__(self) -> int:
+        return len(self.buffers)
+
+
 def _ptrs(xs) -> C.Array:
+    if isinstance(xs, PtrTable):
+        return xs.array
     return (C.c_void_p * len(xs))(*[_addr(x) for x in xs])
 
 
@@ -265,6 +283,13 @@ def zero1_profile_stop(h: int) -> tuple[float, float, int]:
     return a.value, b.value, n.value
 
 
+def zero1_step_launches(h: int) -> int:
+    """Kernel launches per zero1_step: 2, or 1 on the one-launch small-n path."""
+    k = C.c_int()
+    _check(_load().zero1_step_launches(h, C.byref(k)))
+    return k.value
+
+
 def zero1_profile_read(h: int, capacity: int) -> tuple[list[float], list[float]]:
     """Per-step (reduce-scatter+norm ms, update+all-gather ms) recorded so far."""
     a, b, n = (C.c_float * max(1, capacity))(), (C.c_float * max(1, capacity))(), C.c_uint64()
@@ -333,6 +358,9 @@ class Zero1:
 
     def host_sync(self) -> None:
         zero1_host_sync(self.handle)
+
+    def launches_per_step(self) -> int:
+        return zero1_step_launches(self.handle)
 
     def set_state(self, master, m=None, v=None, t: int = 0, stream=None) -> None:
         zero1_set_state(self.handle, master, m, v, t, stream)

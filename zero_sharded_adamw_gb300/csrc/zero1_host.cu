@@ -188,6 +188,7 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         if (opts->size != sizeof(zero1_options)) return fail(ZERO1_EINVAL, "opts->size must be sizeof(zero1_options)");
         if (!finite_nonneg(opts->clip_eps)) return fail(ZERO1_EINVAL, "clip_eps must be finite and >= 0");
         if (opts->bucket_ctas < 0) return fail(ZERO1_EINVAL, "bucket_ctas must be >= 0");
+        if (opts->small_step < -1 || opts->small_step > 1) return fail(ZERO1_EINVAL, "small_step must be -1, 0 or 1");
         o = *opts;
     }
 
@@ -310,6 +311,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.moments_bf16 = h->opts.moments_bf16 != 0;
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
+    s.small_vpt = zero1::small_step_vpt(h->n, h->world, h->opts.small_step);
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
@@ -324,10 +326,7 @@ namespace {
 constexpr int kCopyStreams = 4;
 constexpr uint64_t kCopyChunk = 64ull << 20;
 
-// `count` copies of `bytes` each, cut into chunks of at most 64 MiB and dealt
-// round-robin over the handle's copy streams so that several copy engines
-// run at once; they start after the work already on `st` and the work
-// enqueued on `st` afterwards waits for all of them.
+// Create a lane set's streams and events on first use.
 int lanes_ready(CopyLanes &l)
 {
     if (l.ready) return ZERO1_OK;
@@ -613,6 +612,14 @@ int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, ui
     if (rs_norm_ms) *rs_norm_ms = a;
     if (update_ms) *update_ms = b;
     if (steps) *steps = used;
+    return ZERO1_OK;
+}
+
+int zero1_step_launches(zero1_handle h, int *launches)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!launches) return fail(ZERO1_EINVAL, "launches is NULL");
+    *launches = zero1::small_step_vpt(h->n, h->world, h->opts.small_step) > 0 ? 1 : 2;
     return ZERO1_OK;
 }
 

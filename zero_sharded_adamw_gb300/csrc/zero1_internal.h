@@ -10,6 +10,10 @@ namespace zero1 {
 constexpr int kVec = 8;          // parameters per 16-byte vector of bf16
 constexpr int kThreads = 256;    // threads per CTA, both kernels
 constexpr int kShardAlign = 64;  // shard length multiple (256-byte fp32 shard starts)
+// Automatic one-launch path: at most this many parameters and bytes per step
+// (measured crossover against the two-kernel path on GB300).
+constexpr uint64_t kSmallAutoMaxN = 32768;
+constexpr uint64_t kSmallAutoBytes = 6ull << 20;
 
 // Device-resident result of the norm pass (library-owned, 32 bytes).
 struct DevStatus {
@@ -57,7 +61,28 @@ struct StepLaunch {
     double *bucket_sums = nullptr;  // phase 1: written at [2*bucket_index]; phase 2: read
     int bucket_index = 0;
     int nbuckets = 0;
+    // small steps: > 0 selects the one-launch cluster kernel with this many
+    // 8-parameter vectors per thread (see small_step_vpt)
+    int small_vpt = 0;
 };
+
+// The one-launch path for small n: a cluster of kSmallCtas CTAs of
+// kSmallThreads threads, each thread holding up to kSmallMaxVpt vectors.
+constexpr int kSmallCtas = 8;
+constexpr int kSmallThreads = 256;
+constexpr int kSmallMaxVpt = 4;
+constexpr uint64_t kSmallCap = (uint64_t)kSmallCtas * kSmallThreads * kVec * kSmallMaxVpt;   // 65,536
+
+// Vectors per thread (1, 2 or 4) for the one-launch path, or 0 for the
+// two-kernel path.  mode: 0 = automatic (n and the bytes it moves both
+// small), 1 = whenever n fits (n <= kSmallCap), -1 = never.
+inline int small_step_vpt(uint64_t n, int world, int mode)
+{
+    if (mode < 0 || n > kSmallCap) return 0;
+    if (mode == 0 && (n > kSmallAutoMaxN || n * (4ull * (uint64_t)world + 24ull) > kSmallAutoBytes)) return 0;
+    const uint64_t per = (uint64_t)kSmallCtas * kSmallThreads * kVec;
+    return n <= per ? 1 : n <= 2 * per ? 2 : 4;
+}
 
 // Enqueue the reduce-scatter + norm kernel, then the update + all-gather
 // kernel.  `ev`, when not null, holds three events recorded before, between

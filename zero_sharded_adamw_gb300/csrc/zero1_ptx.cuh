@@ -163,6 +163,29 @@ __device__ __forceinline__ void drain_loads(uint64_t *full, uint32_t issued)
     }
 }
 
+// ------------------------------------------------------ thread-block cluster
+
+// All threads of all CTAs of the cluster arrive and wait (the non-.aligned
+// form: threads need not be converged when they reach it); the release /
+// acquire pair orders every CTA's shared-memory writes before the barrier
+// against reads after it, anywhere in the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The double at the same shared-memory offset as `local`, in the CTA of
+// cluster rank `rank` (distributed shared memory).
+__device__ __forceinline__ double ld_cluster_f64(const double *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    double v;
+    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------ bf16 pack
 
 // bf16 -> fp32 widening is exact: the bf16 bits are the top half.
