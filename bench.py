@@ -227,7 +227,8 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     stream = torch.cuda.current_stream(dev)
 
     hp = z.Hparams(**w.hparams())
-    opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step)
+    opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step,
+                     capturable=args.graph)
     grad_sets = [WL.grads(w, t, dev) for t in (1, 2)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     opt = z.Zero1(w.n, w.world, hp, opts)
@@ -299,6 +300,30 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
                    "launches_timed": prof_steps}
         roof_kernel, roof_bytes, roof_ms = "zero1_adamw_ag_kernel", upd_bytes, upd_avg
 
+    # Graph replay (capturable handle): one captured step replayed K times,
+    # so the host enqueues one graph launch per step instead of the step's
+    # kernel launches and profile events.
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            opt.step(tables[0], rep_table, torch.cuda.current_stream(dev))
+        for _ in range(3):
+            g.replay()
+        barrier(world_size)
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = reduce_max(g0.elapsed_time(g1), world_size, dev)
+        graph = {"ms_per_step": gms / args.steps, "value": world_size * w.n * args.steps / (gms / 1e3),
+                 "unit": "params/s", "steps": args.steps,
+                 "note": "one captured zero1_step (capturable handle) replayed per step; same gradients each step"}
+        del g
+
     # End to end through the host-buffer entry points: every step uploads
     # every rank's gradient from pinned memory, runs the step and downloads
     # every rank's replica.  The pipelined entry point overlaps step t's
@@ -358,7 +383,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
                            # host time to enqueue one step (binding + C ABI + launches + profile
                            # events); when it reaches ms_per_step the GPU waits on the host
                            "host_enqueue_per_step": 1e3 * host_enqueue_s / args.steps},
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "graph_replay": graph,
         "gpu_launches": launches * args.steps,
         "last_step": {"grad_norm": norm, "clip_coef": clip},
     }
@@ -661,6 +686,8 @@ def main(argv=None):
     ap.add_argument("--decay-first", action="store_true", help="variant: torch.optim.AdamW's decay order")
     ap.add_argument("--clip-eps", type=float, default=0.0, help="variant: clip eps (torch uses 1e-6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capturable handle; also time one captured step replayed per step")
     ap.add_argument("--small-step", type=int, default=0, choices=[-1, 0, 1],
                     help="one-launch small-n path: 0 automatic, 1 whenever n fits, -1 never")
     args = ap.parse_args(argv)
@@ -672,7 +699,7 @@ def main(argv=None):
     cfg = {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
            "bytes_per_param": 4 * w.world + (16 if args.moments_bf16 else 24), "hparams": w.hparams(),
            "variant": {"moments_bf16": args.moments_bf16, "decay_first": args.decay_first,
-                       "clip_eps": args.clip_eps, "small_step": args.small_step},
+                       "clip_eps": args.clip_eps, "small_step": args.small_step, "capturable": args.graph},
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
                  else "working set fits in L2 (launch-latency bound)"}

@@ -115,6 +115,19 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     n <= 32,768 and (4W+24)*n <= 6 MiB), 1 = whenever n <= 65,536,
  *     -1 = never.  Either path computes the same update; only the order of
  *     the norm's partial sums differs (see zero1_get_grad_norm).
+ *   capturable: 1 = the step counter t and the learning rate live in
+ *     device memory and the kernels form each step's step size and decay
+ *     there, so zero1_step (and zero1_bucket_finish) can be captured in a
+ *     CUDA graph and replayed: every replay is the next step.  The bias
+ *     corrections 1 - beta^t are tabulated by the host at create time with
+ *     the same double operations as the host path, up to the step where
+ *     both are exactly 1.0 (at most 2^22 steps: 64 MiB; beta2 = 0.99999
+ *     needs 3.7M, beta2 = 0.999999 is refused), so the results equal a
+ *     non-capturable handle's bit for bit.  zero1_set_lr then waits for the
+ *     device; zero1_set_lr_ptr reads lr from a caller's device double
+ *     (for schedules inside a graph); zero1_get_state reads t from the
+ *     device; zero1_set_state writes it.  Profiling (zero1_profile_start)
+ *     must not be active while a step is being captured.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -123,6 +136,7 @@ typedef struct zero1_options {
     int32_t moments_bf16;
     int32_t bucket_ctas;
     int32_t small_step;
+    int32_t capturable;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).
@@ -236,6 +250,15 @@ int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float
  * cosine, "Parallel training", "training loop and checkpoint").
  * Errors: ZERO1_EINVAL for a NULL handle or lr < 0 or not finite. */
 int zero1_set_lr(zero1_handle h, double lr);
+
+/* Capturable handles only: later steps (and replays of captured steps)
+ * read the learning rate from the device double at device_lr, which the
+ * caller may update on the step's stream (e.g. a schedule kernel captured
+ * in the same graph); it must stay valid while such steps run.  NULL goes
+ * back to the handle's own slot (set by zero1_set_lr).
+ * Errors: ZERO1_EINVAL (no handle, or a non-capturable one), ZERO1_EALIGN
+ * (not 8-byte aligned). */
+int zero1_set_lr_ptr(zero1_handle h, const double *device_lr);
 
 /* Norm of the averaged gradient of the latest step and the clip coefficient
  * it applied (1 when not clipped).  Waits for `stream`.  Either output may

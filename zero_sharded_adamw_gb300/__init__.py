@@ -22,7 +22,7 @@ __all__ = [
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
-    "zero1_set_lr", "zero1_get_grad_norm",
+    "zero1_set_lr", "zero1_set_lr_ptr", "zero1_get_grad_norm",
     "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
@@ -48,6 +48,7 @@ _SIGS = {
     "zero1_set_state_range": (_I32, [_P, _U64, _U64, _P, _P, _P, _P]),
     "zero1_get_state_range": (_I32, [_P, _U64, _U64, _P, _P, _P, _P]),
     "zero1_set_lr": (_I32, [_P, _F64]),
+    "zero1_set_lr_ptr": (_I32, [_P, _P]),
     "zero1_get_grad_norm": (_I32, [_P, _P, _P, _P]),
     "zero1_layout": (_I32, [_P, _P, _P, _P]),
     "zero1_bucket_begin": (_I32, [_P]),
@@ -93,23 +94,27 @@ class Hparams:
 
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
-                ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32)]
+                ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32),
+                ("capturable", C.c_int32)]
 
 
 @dataclass
 class Options:
     """Step variants: torch.optim.AdamW's decay order, a clip eps (torch's
     clip_grad_norm_ uses 1e-6), m and v stored in bf16; the bucketed step's
-    CTAs per bucket; the one-launch small-n path (0 auto, 1 on, -1 off)."""
+    CTAs per bucket; the one-launch small-n path (0 auto, 1 on, -1 off);
+    capturable steps (device-side step counter and lr, for CUDA graphs)."""
     decay_before_update: bool = False
     clip_eps: float = 0.0
     moments_bf16: bool = False
     bucket_ctas: int = 0
     small_step: int = 0
+    capturable: bool = False
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
-                         1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step)
+                         1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step,
+                         1 if self.capturable else 0)
 
 
 _lib = None
@@ -246,6 +251,11 @@ def zero1_set_lr(h: int, lr: float) -> None:
     _check(_load().zero1_set_lr(h, lr))
 
 
+def zero1_set_lr_ptr(h: int, device_lr=None) -> None:
+    """Capturable handles: read lr from a device float64 (None: own slot)."""
+    _check(_load().zero1_set_lr_ptr(h, _addr(device_lr)))
+
+
 def zero1_get_grad_norm(h: int, stream=None) -> tuple[float, float]:
     norm, clip = C.c_double(), C.c_float()
     _check(_load().zero1_get_grad_norm(h, C.byref(norm), C.byref(clip), _stream(stream)))
@@ -370,6 +380,9 @@ class Zero1:
 
     def set_lr(self, lr: float) -> None:
         zero1_set_lr(self.handle, lr)
+
+    def set_lr_ptr(self, device_lr=None) -> None:
+        zero1_set_lr_ptr(self.handle, device_lr)
 
     def grad_norm(self, stream=None) -> tuple[float, float]:
         return zero1_get_grad_norm(self.handle, stream)

@@ -23,7 +23,10 @@ HEADERS = [os.path.join(CSRC, "zero1_internal.h"), os.path.join(CSRC, "zero1_ptx
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+# Host code forms the per-step scalars in double; -ffp-contract=off keeps the
+# host compiler from fusing 1 - lr*wd into one FMA (aarch64 has FMA in its
+# base ISA), so the host rounds exactly as the written expression does.
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
                 "-I", INCLUDE, "-I", CSRC]
 
 

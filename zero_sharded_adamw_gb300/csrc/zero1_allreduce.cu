@@ -304,7 +304,7 @@ cudaError_t launch_ar(uint64_t n, int world, int average, const void *const *in,
     if (ntiles < grid) grid = ntiles;
     if (grid < 1) grid = 1;
     auto kern = zero1_allreduce_kernel<T, CAP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ArSmem));
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), (int)sizeof(ArSmem));
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads, sizeof(ArSmem), stream>>>(p);
     return cudaGetLastError();

@@ -19,6 +19,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <set>
 #include <unordered_set>
 #include <algorithm>
 #include <utility>
@@ -58,6 +59,11 @@ struct zero1_ctx {
     void *staging = nullptr;
     uint64_t staging_stride = 0;
     CopyLanes copy;
+    // capturable handles: bias-correction table (1 - beta1^t, 1 - beta2^t)
+    // for t = 1..tab_len on the device, and where the kernels read lr
+    double2 *bctab = nullptr;
+    uint64_t tab_len = 0;
+    const double *lr_ptr = nullptr;
     // pipelined host path (zero1_step_host_async): two staging sets, upload
     // and download lanes, and per set the events its last download recorded
     void *astaging = nullptr;
@@ -140,6 +146,21 @@ zero1::StepScalars step_scalars(const zero1_hparams &hp, int world, uint64_t t)
     return s;
 }
 
+constexpr uint64_t kMaxBiasTable = 1ull << 22;   // entries (64 MiB) a capturable handle may tabulate
+
+// The step's scalars as a capturable launch forms them on the device.
+zero1::DevScalars dev_scalars(const zero1_ctx *h)
+{
+    zero1::DevScalars d{};
+    if (h->bctab) {
+        d.bc = h->bctab;
+        d.tab_len = h->tab_len;
+        d.lr = h->lr_ptr;
+        d.weight_decay = h->hp.weight_decay;
+    }
+    return d;
+}
+
 // Make the handle's device current for the duration of a call.
 struct DeviceGuard {
     int prev = -1;
@@ -161,6 +182,25 @@ void zero1::set_error_message(const char *msg)
     snprintf(g_err, sizeof g_err, "%s", msg);
 }
 
+cudaError_t zero1::allow_dynamic_smem(const void *kernel, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (done.count({kernel, dev})) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lk(mu);
+        done.insert({kernel, dev});
+    }
+    return e;
+}
+
 extern "C" {
 
 const char *zero1_last_error(void) { return g_err; }
@@ -168,6 +208,37 @@ const char *zero1_last_error(void) { return g_err; }
 int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *out)
 {
     return zero1_create_ex(n, world, hp, nullptr, out);
+}
+
+// Capturable handles: tabulate the two bias corrections exactly as
+// step_scalars forms them, up to the first t at which both are 1.0 in
+// double (they stay 1.0 after it), and seed the device lr slot and t = 0.
+static int build_bias_table(zero1_ctx *h)
+{
+    std::vector<double2> tab;
+    for (uint64_t t = 1;; ++t) {
+        if (t > kMaxBiasTable)
+            return fail(ZERO1_EINVAL, "capturable: the bias corrections do not reach 1.0 within %llu steps",
+                        (unsigned long long)kMaxBiasTable);
+        const double bc1 = 1.0 - std::pow(h->hp.beta1, (double)t);
+        const double bc2 = 1.0 - std::pow(h->hp.beta2, (double)t);
+        tab.push_back(make_double2(bc1, bc2));
+        if (bc1 == 1.0 && bc2 == 1.0) break;
+    }
+    cudaError_t e;
+    if ((e = cudaMalloc(&h->bctab, tab.size() * sizeof(double2))) != cudaSuccess) {
+        h->bctab = nullptr;
+        return cuda_fail(e, "cudaMalloc of the bias-correction table");
+    }
+    if ((e = cudaMemcpy(h->bctab, tab.data(), tab.size() * sizeof(double2), cudaMemcpyHostToDevice)) != cudaSuccess ||
+        (e = cudaMemcpy(&h->status->lr, &h->hp.lr, sizeof(double), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(h->bctab);
+        h->bctab = nullptr;
+        return cuda_fail(e, "bias-correction table upload");
+    }
+    h->tab_len = tab.size();
+    h->lr_ptr = &h->status->lr;
+    return ZERO1_OK;
 }
 
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts, zero1_handle *out)
@@ -189,6 +260,7 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         if (!finite_nonneg(opts->clip_eps)) return fail(ZERO1_EINVAL, "clip_eps must be finite and >= 0");
         if (opts->bucket_ctas < 0) return fail(ZERO1_EINVAL, "bucket_ctas must be >= 0");
         if (opts->small_step < -1 || opts->small_step > 1) return fail(ZERO1_EINVAL, "small_step must be -1, 0 or 1");
+        if (opts->capturable != 0 && opts->capturable != 1) return fail(ZERO1_EINVAL, "capturable must be 0 or 1");
         o = *opts;
     }
 
@@ -241,6 +313,14 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         delete h;
         return cuda_fail(e, "cudaMemset of optimizer state");
     }
+    if (o.capturable) {
+        rc = build_bias_table(h);
+        if (rc) {
+            cudaFree(h->block);
+            delete h;
+            return rc;
+        }
+    }
     {
         std::lock_guard<std::mutex> lk(g_mu);
         g_live.insert(h);
@@ -275,6 +355,7 @@ int zero1_destroy(zero1_handle h)
         for (cudaEvent_t ev : set)
             if (ev) cudaEventDestroy(ev);
     if (h->astaging) cudaFree(h->astaging);
+    if (h->bctab) cudaFree(h->bctab);
     delete h;
     if (e1 != cudaSuccess) return cuda_fail(e1, "cudaDeviceSynchronize in destroy");
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
@@ -312,6 +393,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
     s.small_vpt = zero1::small_step_vpt(h->n, h->world, h->opts.small_step);
+    s.dev = dev_scalars(h);
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
@@ -524,6 +606,14 @@ int zero1_set_state(zero1_handle h, const float *master, const void *m, const vo
     int rc = zero1_set_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
     if (rc) return rc;
     h->t = t;
+    if (h->bctab) {   // capturable: the device counter is the step count
+        DeviceGuard g(h->device);
+        const unsigned long long tt = t;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemcpyAsync(&h->status->t, &tt, sizeof tt, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "step counter write");
+    }
     return ZERO1_OK;
 }
 
@@ -531,6 +621,15 @@ int zero1_get_state(zero1_handle h, float *master, void *m, void *v, uint64_t *t
 {
     int rc = zero1_get_state_range(h, 0, h && live(h) ? h->n : 0, master, m, v, stream);
     if (rc) return rc;
+    if (t && h->bctab) {   // capturable: read the device counter (replayed graphs advance it)
+        DeviceGuard g(h->device);
+        unsigned long long tt = 0;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemcpyAsync(&tt, &h->status->t, sizeof tt, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "step counter read");
+        h->t = tt;
+    }
     if (t) *t = h->t;
     return ZERO1_OK;
 }
@@ -540,6 +639,22 @@ int zero1_set_lr(zero1_handle h, double lr)
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (!finite_nonneg(lr)) return fail(ZERO1_EINVAL, "lr must be finite and >= 0");
     h->hp.lr = lr;
+    if (h->bctab) {   // capturable: the handle's device lr slot, after all queued work
+        DeviceGuard g(h->device);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaMemcpy(&h->status->lr, &lr, sizeof lr, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "lr write");
+    }
+    return ZERO1_OK;
+}
+
+int zero1_set_lr_ptr(zero1_handle h, const double *device_lr)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (!h->bctab) return fail(ZERO1_EINVAL, "zero1_set_lr_ptr needs a capturable handle");
+    if (device_lr && (reinterpret_cast<uintptr_t>(device_lr) & 7u))
+        return fail(ZERO1_EALIGN, "device_lr is not 8-byte aligned");
+    h->lr_ptr = device_lr ? device_lr : &h->status->lr;
     return ZERO1_OK;
 }
 
@@ -745,6 +860,7 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
     s.phase = 2;
+    s.dev = dev_scalars(h);
     s.bucket_sums = h->bucket_sums;
     s.nbuckets = (int)h->buckets.size();
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), nullptr);

@@ -15,7 +15,8 @@ constexpr int kShardAlign = 64;  // shard length multiple (256-byte fp32 shard s
 constexpr uint64_t kSmallAutoMaxN = 32768;
 constexpr uint64_t kSmallAutoBytes = 6ull << 20;
 
-// Device-resident result of the norm pass (library-owned, 32 bytes).
+// Device-resident result of the norm pass and, for capturable handles, the
+// step counter and learning rate (library-owned).
 struct DevStatus {
     double nsq;        // sum of squares of the averaged gradient
     double norm;       // sqrt(nsq)
@@ -23,6 +24,21 @@ struct DevStatus {
     unsigned ticket;   // last-CTA election counter; 0 between launches
     unsigned flags;    // bit 0: the norm is not finite (rewritten every step)
     unsigned errors;   // sticky: bit 0 = a pipeline wait gave up (1 s limit)
+    unsigned long long t;  // capturable: steps taken (the update kernel's last CTA advances it)
+    double lr;             // capturable: the handle's own learning-rate slot
+    unsigned ticket2;      // capturable: update-kernel CTA counter; 0 between launches
+    unsigned pad;
+};
+
+// Capturable steps: the step size and decay are formed on the device from
+// the step counter in DevStatus, a learning rate read through lr, and the
+// bias corrections (1 - beta1^t, 1 - beta2^t) tabulated by the host for
+// t = 1..tab_len (both are exactly 1.0 in double from t = tab_len on).
+struct DevScalars {
+    const double2 *bc;     // nullptr: the launch's host-formed scalars are used
+    uint64_t tab_len;
+    const double *lr;
+    double weight_decay;
 };
 constexpr unsigned kFlagNonFinite = 1u;
 constexpr unsigned kErrWaitTimeout = 1u;
@@ -64,6 +80,7 @@ struct StepLaunch {
     // small steps: > 0 selects the one-launch cluster kernel with this many
     // 8-parameter vectors per thread (see small_step_vpt)
     int small_vpt = 0;
+    DevScalars dev{};       // capturable handles
 };
 
 // The one-launch path for small n: a cluster of kSmallCtas CTAs of
@@ -88,6 +105,12 @@ inline int small_step_vpt(uint64_t n, int world, int mode)
 // kernel.  `ev`, when not null, holds three events recorded before, between
 // and after the two kernels.
 cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev);
+
+// cudaFuncSetAttribute(kernel, max dynamic shared memory, bytes) once per
+// (kernel, device): the attribute stays with the context, and skipping the
+// call keeps a step's host path short and free of non-stream calls (so a
+// step can be captured in a CUDA graph after one uncaptured step).
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
 
 // Grid sizes: one wave of resident CTAs on this device, capped by the work.
 void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);

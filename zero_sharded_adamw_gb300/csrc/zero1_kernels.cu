@@ -92,6 +92,7 @@ struct UpdParams {
     const double *bucket_sums;   // bucketed step: c comes from these nbuckets pairs
     int nbuckets;
     double max_norm, clip_eps;
+    DevScalars dev;              // capturable: scalars formed from the device step counter
 };
 
 // Scalar rank-ordered sum for the last n % 8 parameters.
@@ -176,6 +177,22 @@ __device__ __forceinline__ void finish_norm(double x, double y, double max_norm,
         status->flags = isfinite(norm) ? 0u : kFlagNonFinite;
     }
     *clip_out = c;
+}
+
+// The step's scalars on a capturable handle: the host-formed constants with
+// the step size lr * sqrt(1 - beta2^t) / (1 - beta1^t) and the decay
+// 1 - lr * weight_decay formed here for step t, in the same double
+// operations, in the same order, as the host forms them (so both give the
+// same fp32 values bit for bit).
+__device__ __forceinline__ StepScalars form_scalars(const StepScalars &base, const DevScalars &d, unsigned long long t)
+{
+    const uint64_t i = (t < d.tab_len ? t : d.tab_len) - 1;
+    const double2 bc = d.bc[i];
+    const double lr = *d.lr;
+    StepScalars s = base;
+    s.step_size = __double2float_rn(__ddiv_rn(__dmul_rn(lr, __dsqrt_rn(bc.y)), bc.x));
+    s.decay = __double2float_rn(__dsub_rn(1.0, __dmul_rn(lr, d.weight_decay)));
+    return s;
 }
 
 // ------------------------------------------------------------------- K1
@@ -398,6 +415,7 @@ struct UpdSmem {
     uint64_t full[kUpdStages], done[kUpdStages], empty[kUpdStages];
     int abort;
     float clip;
+    StepScalars sc;
 };
 
 // Four consecutive parameters at offset o of stage s: AdamW in place on the
@@ -497,6 +515,19 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         } else {
             sm.clip = p.status->clip;
         }
+        if (p.dev.bc) {
+            // Capturable: this step is t + 1.  The CTA that counts in last
+            // (every CTA has read t by then) advances the counter.
+            const unsigned long long t = p.status->t + 1;
+            sm.sc = form_scalars(p.sc, p.dev, t);
+            __threadfence();
+            if (atomicAdd(&p.status->ticket2, 1u) == gridDim.x - 1) {
+                p.status->t = t;
+                p.status->ticket2 = 0u;
+            }
+        } else {
+            sm.sc = p.sc;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -567,6 +598,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     // of every tile, so a warp's 16-byte shared-memory accesses are
     // consecutive (no bank conflicts).
     const float c = sm.clip;
+    const StepScalars sc = sm.sc;
     const uint32_t o0 = threadIdx.x * 4u, o1 = kTile / 2 + threadIdx.x * 4u;
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
@@ -581,8 +613,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             // line may hold the n % 8 tail and is left alone).
             discard_l2_line(p.ghat + base + threadIdx.x * 32u);
         }
-        if (o0 < cnt) update4<REREAD, MV16>(sm, s, o0, nw, c, p.sc, p.decay_first != 0);
-        if (o1 < cnt) update4<REREAD, MV16>(sm, s, o1, nw, c, p.sc, p.decay_first != 0);
+        if (o0 < cnt) update4<REREAD, MV16>(sm, s, o0, nw, c, sc, p.decay_first != 0);
+        if (o1 < cnt) update4<REREAD, MV16>(sm, s, o1, nw, c, sc, p.decay_first != 0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.done[s]);
@@ -600,7 +632,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
             m = static_cast<const float *>(p.m)[e];
             v = static_cast<const float *>(p.v)[e];
         }
-        adamw1<MV16>(gh, c, p.sc, p.decay_first != 0, w, m, v);
+        adamw1<MV16>(gh, c, sc, p.decay_first != 0, w, m, v);
         p.master[e] = w;
         if (MV16) {
             static_cast<__nv_bfloat16 *>(p.m)[e] = __float2bfloat16_rn(m);
@@ -638,6 +670,7 @@ struct SmallParams {
     int decay_first;
     StepScalars sc;
     double max_norm, clip_eps;
+    DevScalars dev;
 };
 
 template <bool MV16>
@@ -675,10 +708,15 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
     __shared__ double red_a[kWarps], red_b[kWarps];
     __shared__ double part[2];
     __shared__ float clip;
+    __shared__ StepScalars ssc;
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
     const uint32_t gt = blockIdx.x * kSmallThreads + threadIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Capturable: this step is t + 1; every CTA reads t here, before the
+    // first cluster barrier, and CTA 0 advances it after the second.
+    const unsigned long long tnext = p.dev.bc ? p.status->t + 1 : 0ull;
+    if (threadIdx.x == 0) ssc = p.dev.bc ? form_scalars(p.sc, p.dev, tnext) : p.sc;
 
     float gh[VPT][8], w[VPT][8], m[VPT][8], v[VPT][8];
     uint64_t ev[VPT];
@@ -786,14 +824,16 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
     }
     cluster_sync();            // all remote reads are done (no CTA leaves early); `clip` is visible
     const float c = clip;
+    const StepScalars sc = ssc;
     const bool decay_first = p.decay_first != 0;
+    if (p.dev.bc && blockIdx.x == 0 && threadIdx.x == 0) p.status->t = tnext;
 
 #pragma unroll
     for (int q = 0; q < VPT; ++q) {
         const uint64_t e = (uint64_t)(gt + q * kStride) * kVec;
         if (e < nel) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) adamw1<MV16>(gh[q][k], c, p.sc, decay_first, w[q][k], m[q][k], v[q][k]);
+            for (int k = 0; k < 8; ++k) adamw1<MV16>(gh[q][k], c, sc, decay_first, w[q][k], m[q][k], v[q][k]);
             store_moment8<false>(p.master, e, w[q]);
             store_moment8<MV16>(p.m, e, m[q]);
             store_moment8<MV16>(p.v, e, v[q]);
@@ -803,7 +843,7 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
         }
     }
     if (tail) {
-        adamw1<MV16>(tg, c, p.sc, decay_first, tw, tm, tv);
+        adamw1<MV16>(tg, c, sc, decay_first, tw, tm, tv);
         p.master[et] = tw;
         if (MV16) {
             static_cast<__nv_bfloat16 *>(p.m)[et] = __float2bfloat16_rn(tm);
@@ -822,7 +862,7 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
 template <typename Kernel>
 cudaError_t allow_smem(Kernel kernel, size_t bytes)
 {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    return allow_dynamic_smem(reinterpret_cast<const void *>(kernel), (int)bytes);
 }
 
 template <int W, int CAP, int VPT, bool MV16>
@@ -844,6 +884,7 @@ cudaError_t launch_small_v(const StepLaunch &s, cudaStream_t stream)
     sp.sc = s.sc;
     sp.max_norm = s.max_norm;
     sp.clip_eps = s.clip_eps;
+    sp.dev = s.dev;
     zero1_small_step_kernel<W, CAP, VPT, MV16><<<kSmallCtas, kSmallThreads, 0, stream>>>(sp);
     return cudaGetLastError();
 }
@@ -907,6 +948,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     up.nbuckets = s.nbuckets;
     up.max_norm = s.max_norm;
     up.clip_eps = s.clip_eps;
+    up.dev = s.dev;
 
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
