@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import datetime as dt
 import hashlib
+import re
 import json
 import os
 import shutil
@@ -39,7 +40,23 @@ import workloads as WL  # noqa: E402
 
 METRIC = "ZeRO-1 step params/s and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "zero_sharded_adamw_gb300", "csrc", "zero1_kernels.cu")
+CSRC = os.path.join(ROOT, "zero_sharded_adamw_gb300", "csrc")
+# The sources the step's kernels are compiled from; a committed ncu summary
+# counts for the current build only if it carries their digest.
+KERNEL_SRCS = [os.path.join(CSRC, f) for f in ("zero1_kernels.cu", "zero1_ptx.cuh", "zero1_internal.h")]
+
+
+def kernel_source_digest(paths=KERNEL_SRCS) -> str:
+    """sha256 over the sources with comments and whitespace runs removed, so
+    that an edit to a comment does not orphan counters taken on the same code."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()
 
 
 # ------------------------------------------------------------- helpers
@@ -94,8 +111,7 @@ def kernel_traffic(workload: str) -> tuple[float | None, str | None]:
     the full-size one-pass capture of the workload if there is one, else a
     small-case capture scaled to the workload's size.  (None, None) when
     neither matches the current source."""
-    with open(KERNEL_SRC, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+    sha = kernel_source_digest()
     name = workload.replace("@", "_n")
     for fname, key in ((f"dram_{name}.txt", "zero1_adamw_ag_kernel.dram_bytes_per_launch"),
                        (f"zero1_adamw_ag_kernel_{name}.txt", "dram_bytes_per_launch")):
@@ -103,7 +119,7 @@ def kernel_traffic(workload: str) -> tuple[float | None, str | None]:
         if not os.path.exists(path):
             continue
         fields = _summary_fields(path)
-        if fields.get("kernel_source_sha256") != sha:
+        if fields.get("kernel_source_digest") != sha:
             continue
         try:
             return float(fields[key]), "profiles/" + fname

@@ -1,5 +1,6 @@
 // zero1_internal.h -- declarations shared by the C-ABI host code
-// (zero1_host.cu) and the two kernels (zero1_kernels.cu).  Not installed.
+// (zero1_host.cu, zero1_noalloc.cu, zero1_allreduce.cu) and the step's
+// kernels (zero1_kernels.cu).  Not installed.
 #pragma once
 
 #include <cstdint>
@@ -8,7 +9,6 @@
 namespace zero1 {
 
 constexpr int kVec = 8;          // parameters per 16-byte vector of bf16
-constexpr int kThreads = 256;    // threads per CTA, both kernels
 constexpr int kShardAlign = 64;  // shard length multiple (256-byte fp32 shard starts)
 // Automatic one-launch path: at most this many parameters and bytes per step
 // (measured crossover against the two-kernel path on GB300).
@@ -102,8 +102,9 @@ inline int small_step_vpt(uint64_t n, int world, int mode)
 }
 
 // Enqueue the reduce-scatter + norm kernel, then the update + all-gather
-// kernel.  `ev`, when not null, holds three events recorded before, between
-// and after the two kernels.
+// kernel (or, when small_vpt > 0, the one-launch kernel).  `ev`, when not
+// null, holds three events recorded before, between and after the two
+// kernels (before, after and after the one-launch kernel).
 cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev);
 
 // cudaFuncSetAttribute(kernel, max dynamic shared memory, bytes) once per

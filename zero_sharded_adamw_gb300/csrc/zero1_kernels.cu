@@ -1,4 +1,4 @@
-// zero1_kernels.cu -- the two sm_103a kernels of one ZeRO-1 step.
+// zero1_kernels.cu -- the sm_103a kernels of one ZeRO-1 step.
 //
 //  K1  zero1_rs_norm_kernel   reduce-scatter (rank-ordered fp32 sum of the W
 //                             bf16 gradients, times 1/W) fused with the
@@ -7,6 +7,8 @@
 //                             CTA, which also forms the clip coefficient.
 //  K2  zero1_adamw_ag_kernel  clip scale + AdamW on fp32 master/m/v + bf16
 //                             cast + all-gather (W-way store of each tile).
+//  K0  zero1_small_step_kernel  all of the above in one launch of one
+//                             8-CTA thread-block cluster, for small n.
 //
 // Sources (web pages, cited by title and section):
 //  "Stanford CS336 Lecture 7 close reading: Parallelism (part 1)", 5.2: the
