@@ -23,11 +23,12 @@ HEADERS = [os.path.join(CSRC, "zero1_internal.h"), os.path.join(CSRC, "zero1_ptx
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# ZERO1_NVCC_EXTRA (environment) appends flags, e.g. -D overrides for tuning.
 # Host code forms the per-step scalars in double; -ffp-contract=off keeps the
 # host compiler from fusing 1 - lr*wd into one FMA (aarch64 has FMA in its
 # base ISA), so the host rounds exactly as the written expression does.
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
-                "-I", INCLUDE, "-I", CSRC]
+                "-I", INCLUDE, "-I", CSRC] + os.environ.get("ZERO1_NVCC_EXTRA", "").split()
 
 
 def _stale() -> bool:

@@ -49,13 +49,23 @@ namespace {
 using namespace ptx;
 
 constexpr int kTile = 2048;                      // parameters per tile
-constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel
-constexpr int kUpdStages = 4;                    // shared-memory ring depth, update kernel
+constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel (3 and 2 measured slower)
+// The update kernel's ring depth and consumer warps, per path (measured on
+// GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment workloads): with an
+// fp32 scratch and fp32 moments the kernel is write-heavy (16 B read, 24 + 2W
+// written per parameter) and runs fastest with 3 stages in flight and 16
+// consumer warps; the gradient re-read (W <= 2) and bf16-moment paths run
+// fastest with 4 stages and 8 warps.
+struct UpdConfig {
+    int stages, warps;
+};
+constexpr UpdConfig kUpdSpillF32{3, 16};
+constexpr UpdConfig kUpdDefault{4, 8};
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kRsThreads = kConsumers + 32;      // + producer warp
-constexpr int kUpdThreads = kConsumers + 64;     // + producer warp + store warp
+constexpr int kUpdTile = kTile;                  // parameters per update-kernel tile
 static_assert(kConsumers * kVec == kTile, "one 8-parameter vector per consumer thread");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -410,11 +420,12 @@ __device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, 
     v = vi;
 }
 
+template <int STAGES>
 struct UpdSmem {
-    float in[kUpdStages][4][kTile];   // 32 KB per stage: ghat (or the W <= 2 bf16 grads), master, m, v
+    float in[STAGES][4][kUpdTile];   // 32 KB per stage: ghat (or the W <= 2 bf16 grads), master, m, v
                                    // (m, v use half their slot when stored in bf16)
-    uint16_t b16[kUpdStages][kTile];  // 4 KB per stage: the tile's bf16 parameters
-    uint64_t full[kUpdStages], done[kUpdStages], empty[kUpdStages];
+    uint16_t b16[STAGES][kUpdTile];  // 4 KB per stage: the tile's bf16 parameters
+    uint64_t full[STAGES], done[STAGES], empty[STAGES];
     int abort;
     float clip;
     StepScalars sc;
@@ -422,8 +433,8 @@ struct UpdSmem {
 
 // Four consecutive parameters at offset o of stage s: AdamW in place on the
 // staged master, m, v and the bf16 values into the replica tile.
-template <bool REREAD, bool MV16>
-__device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc,
+template <bool REREAD, bool MV16, int STAGES>
+__device__ __forceinline__ void update4(UpdSmem<STAGES> &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc,
                                         bool decay_first)
 {
     float gh[4];
@@ -435,7 +446,7 @@ __device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, 
         gh[2] = __uint_as_float(raw.y << 16);
         gh[3] = __uint_as_float(raw.y & 0xFFFF0000u);
         for (int r = 1; r < nw; ++r) {
-            raw = *reinterpret_cast<const uint2 *>(g + r * kTile + o);
+            raw = *reinterpret_cast<const uint2 *>(g + r * kUpdTile + o);
             gh[0] = __fadd_rn(gh[0], __uint_as_float(raw.x << 16));
             gh[1] = __fadd_rn(gh[1], __uint_as_float(raw.x & 0xFFFF0000u));
             gh[2] = __fadd_rn(gh[2], __uint_as_float(raw.y << 16));
@@ -484,16 +495,22 @@ __device__ __forceinline__ void update4(UpdSmem &sm, int s, uint32_t o, int nw, 
 // from the highest down (the reduce-scatter kernel wrote those last, so
 // they are the likeliest to still be in L2).  master, m, v are updated in
 // place in the stage and written back from there.
-template <int W, int CAP, bool REREAD, bool MV16>
-__global__ void __launch_bounds__(kUpdThreads, 1)
+template <int W, int CAP, bool REREAD, bool MV16, int STAGES, int CWARPS>
+__global__ void __launch_bounds__(CWARPS * 32 + 64, 1)
 zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 {
     constexpr uint32_t kMomBytes = MV16 ? 2u : 4u;   // bytes per stored moment
+    constexpr int kUpdStages = STAGES;
+    constexpr int kUpdConsumerWarps = CWARPS;
+    constexpr int kUpdConsumers = CWARPS * 32;
+    constexpr int kUpdQuads = kUpdTile / (4 * kUpdConsumers);   // 4-parameter groups per consumer thread per tile
+    static_assert(kUpdQuads >= 1 && kUpdQuads * 4 * kUpdConsumers == kUpdTile, "update consumers must tile kUpdTile");
+    static_assert(kUpdTile / 32 <= kUpdConsumers, "one discarded scratch line per consumer thread");
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    UpdSmem &sm = *reinterpret_cast<UpdSmem *>(smem_raw);
+    UpdSmem<STAGES> &sm = *reinterpret_cast<UpdSmem<STAGES> *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
-    const int64_t ntiles = (int64_t)((nel + kTile - 1) / kTile);
+    const int64_t ntiles = (int64_t)((nel + kUpdTile - 1) / kUpdTile);
     const int64_t first = ntiles - 1 - (int64_t)blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
@@ -501,7 +518,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kUpdStages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.done[s], kConsumerWarps);
+            mbar_init(&sm.done[s], kUpdConsumerWarps);
             mbar_init(&sm.empty[s], 1);
         }
         sm.abort = 0;
@@ -537,20 +554,20 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     // Every byte this kernel moves is touched once per step: lowest L2 priority.
     const uint64_t once = policy_evict_first();
 
-    if (warp == kConsumerWarps) {                                 // producer
+    if (warp == kUpdConsumerWarps) {                              // producer
         if (lane == 0) {
             uint32_t k = 0;
             for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
                 const int s = k % kUpdStages;
                 if (k >= kUpdStages && !mbar_wait(&sm.empty[s], ((k / kUpdStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
-                const uint64_t base = (uint64_t)j * kTile;
-                const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+                const uint64_t base = (uint64_t)j * kUpdTile;
+                const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kUpdTile ? nel - base : kUpdTile);
                 const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
                 mbar_arrive_expect_tx(&sm.full[s], gbytes + 4u * cnt + 2u * kMomBytes * cnt);
                 if (REREAD) {
                     uint16_t *g = reinterpret_cast<uint16_t *>(sm.in[s][0]);
                     for (int r = 0; r < nw; ++r)
-                        tma_load_hint(g + r * kTile, p.grads[r] + base, cnt * 2u, &sm.full[s], once);
+                        tma_load_hint(g + r * kUpdTile, p.grads[r] + base, cnt * 2u, &sm.full[s], once);
                 } else {
                     tma_load_hint(sm.in[s][0], p.ghat + base, cnt * 4u, &sm.full[s], once);
                 }
@@ -565,14 +582,14 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         return;
     }
 
-    if (warp == kConsumerWarps + 1) {                             // stores
+    if (warp == kUpdConsumerWarps + 1) {                          // stores
         uint32_t k = 0;
         for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
             const int s = k % kUpdStages;
             const bool got = mbar_wait(&sm.done[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
-            const uint64_t base = (uint64_t)j * kTile;
-            const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+            const uint64_t base = (uint64_t)j * kUpdTile;
+            const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kUpdTile ? nel - base : kUpdTile);
             // Targets 0..2 are master, m, v; 3.. are the W replicas (the
             // all-gather).  Lane L issues targets L, L+32, ...
             for (int t = lane; t < nw + 3; t += 32) {
@@ -596,27 +613,29 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         return;
     }
 
-    // Consumers: thread t owns parameters [4t, 4t+4) and [1024+4t, 1024+4t+4)
-    // of every tile, so a warp's 16-byte shared-memory accesses are
-    // consecutive (no bank conflicts).
+    // Consumers: thread t owns parameters [4t + 4qC, 4t + 4qC + 4) of every
+    // tile (C consumer threads, q < kUpdQuads), so a warp's 16-byte
+    // shared-memory accesses are consecutive (no bank conflicts).
     const float c = sm.clip;
     const StepScalars sc = sm.sc;
-    const uint32_t o0 = threadIdx.x * 4u, o1 = kTile / 2 + threadIdx.x * 4u;
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
         const int s = k % kUpdStages;
         const bool got = mbar_wait(&sm.full[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
-        const uint64_t base = (uint64_t)j * kTile;
-        const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+        const uint64_t base = (uint64_t)j * kUpdTile;
+        const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kUpdTile ? nel - base : kUpdTile);
         if (!REREAD && threadIdx.x < cnt / 32u) {
             // This tile's ĝ is in shared memory now and dead in HBM: drop its
             // whole 128-byte lines from L2 unwritten (a partly covered last
             // line may hold the n % 8 tail and is left alone).
             discard_l2_line(p.ghat + base + threadIdx.x * 32u);
         }
-        if (o0 < cnt) update4<REREAD, MV16>(sm, s, o0, nw, c, sc, p.decay_first != 0);
-        if (o1 < cnt) update4<REREAD, MV16>(sm, s, o1, nw, c, sc, p.decay_first != 0);
+#pragma unroll
+        for (int q = 0; q < kUpdQuads; ++q) {
+            const uint32_t o = threadIdx.x * 4u + (uint32_t)q * 4u * kUpdConsumers;
+            if (o < cnt) update4<REREAD, MV16, STAGES>(sm, s, o, nw, c, sc, p.decay_first != 0);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.done[s]);
@@ -955,10 +974,18 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
     auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
-    auto k2 = spill ? (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, false, true> : zero1_adamw_ag_kernel<W, CAP, false, false>)
-                    : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true> : zero1_adamw_ag_kernel<W, CAP, true, false>);
+    // fp32 scratch + fp32 moments: kUpdSpillF32; otherwise kUpdDefault.
+    constexpr int S1 = kUpdSpillF32.stages, C1 = kUpdSpillF32.warps;
+    constexpr int S0 = kUpdDefault.stages, C0 = kUpdDefault.warps;
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
-    if ((e = allow_smem(k2, sizeof(UpdSmem))) != cudaSuccess) return e;
+    const bool fast = spill && !s.moments_bf16;
+    auto k2 = fast ? zero1_adamw_ag_kernel<W, CAP, false, false, S1, C1>
+                   : spill ? zero1_adamw_ag_kernel<W, CAP, false, true, S0, C0>
+                           : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true, S0, C0>
+                                             : zero1_adamw_ag_kernel<W, CAP, true, false, S0, C0>);
+    const size_t k2_smem = fast ? sizeof(UpdSmem<S1>) : sizeof(UpdSmem<S0>);
+    const int k2_threads = (fast ? C1 : C0) * 32 + 64;
+    if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
     if (s.phase != 2) {
         k1<<<s.grid_rs, kRsThreads, sizeof(RsSmem), stream>>>(rp);
@@ -966,7 +993,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
     if (s.phase != 1) {
-        k2<<<s.grid_update, kUpdThreads, sizeof(UpdSmem), stream>>>(up);
+        k2<<<s.grid_update, k2_threads, k2_smem, stream>>>(up);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
@@ -1003,7 +1030,11 @@ void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, i
     if (ntiles < g) g = ntiles;
     if (g < 1) g = 1;
     *grid_rs = (int)g;
-    *grid_update = (int)g;
+    const uint64_t ntiles_upd = (n / kVec * kVec + kUpdTile - 1) / kUpdTile;
+    uint64_t gu = (uint64_t)num_sms;
+    if (ntiles_upd < gu) gu = ntiles_upd;
+    if (gu < 1) gu = 1;
+    *grid_update = (int)gu;
 }
 
 }  // namespace zero1
