@@ -59,8 +59,22 @@ constexpr int kStages = 4;                       // shared-memory ring depth, re
 struct UpdConfig {
     int stages, warps;
 };
-constexpr UpdConfig kUpdSpillF32{3, 16};
-constexpr UpdConfig kUpdDefault{4, 8};
+// (-D overrides for tuning: ZERO1_UPD_<PATH>_STAGES / _WARPS.)
+#ifndef ZERO1_UPD_SPILL_F32_STAGES
+#define ZERO1_UPD_SPILL_F32_STAGES 3
+#define ZERO1_UPD_SPILL_F32_WARPS 16
+#endif
+#ifndef ZERO1_UPD_SPILL_BF16_STAGES
+#define ZERO1_UPD_SPILL_BF16_STAGES 4
+#define ZERO1_UPD_SPILL_BF16_WARPS 8
+#endif
+#ifndef ZERO1_UPD_REREAD_STAGES
+#define ZERO1_UPD_REREAD_STAGES 4
+#define ZERO1_UPD_REREAD_WARPS 8
+#endif
+constexpr UpdConfig kUpdSpillF32{ZERO1_UPD_SPILL_F32_STAGES, ZERO1_UPD_SPILL_F32_WARPS};      // fp32 scratch, fp32 moments
+constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_STAGES, ZERO1_UPD_SPILL_BF16_WARPS};   // fp32 scratch, bf16 moments
+constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS};              // gradients re-read (W <= 2)
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
@@ -974,17 +988,17 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
     auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
-    // fp32 scratch + fp32 moments: kUpdSpillF32; otherwise kUpdDefault.
     constexpr int S1 = kUpdSpillF32.stages, C1 = kUpdSpillF32.warps;
-    constexpr int S0 = kUpdDefault.stages, C0 = kUpdDefault.warps;
+    constexpr int S2 = kUpdSpillBf16.stages, C2 = kUpdSpillBf16.warps;
+    constexpr int S0 = kUpdReread.stages, C0 = kUpdReread.warps;
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
-    const bool fast = spill && !s.moments_bf16;
-    auto k2 = fast ? zero1_adamw_ag_kernel<W, CAP, false, false, S1, C1>
-                   : spill ? zero1_adamw_ag_kernel<W, CAP, false, true, S0, C0>
-                           : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true, S0, C0>
-                                             : zero1_adamw_ag_kernel<W, CAP, true, false, S0, C0>);
-    const size_t k2_smem = fast ? sizeof(UpdSmem<S1>) : sizeof(UpdSmem<S0>);
-    const int k2_threads = (fast ? C1 : C0) * 32 + 64;
+    const int path = spill ? (s.moments_bf16 ? 2 : 1) : 0;
+    auto k2 = path == 1   ? zero1_adamw_ag_kernel<W, CAP, false, false, S1, C1>
+              : path == 2 ? zero1_adamw_ag_kernel<W, CAP, false, true, S2, C2>
+                          : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true, S0, C0>
+                                            : zero1_adamw_ag_kernel<W, CAP, true, false, S0, C0>);
+    const size_t k2_smem = path == 1 ? sizeof(UpdSmem<S1>) : path == 2 ? sizeof(UpdSmem<S2>) : sizeof(UpdSmem<S0>);
+    const int k2_threads = (path == 1 ? C1 : path == 2 ? C2 : C0) * 32 + 64;
     if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
     if (s.phase != 2) {
