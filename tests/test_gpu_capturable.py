@@ -37,7 +37,7 @@ def _same(a, b):
         assert bits_equal(x, y)
 
 
-SHAPES = [(100_003, 8), (4099, 4), (70_001, 2)]   # two kernels (W >= 3, W <= 2) and the one-launch path
+SHAPES = [(100_003, 8), (4099, 4), (4096, 4), (70_001, 2)]   # two kernels (W >= 3, W <= 2), the one-launch cluster and one-CTA paths
 
 
 @pytest.mark.parametrize("n,world", SHAPES)

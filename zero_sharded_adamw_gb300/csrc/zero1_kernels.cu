@@ -734,19 +734,19 @@ __device__ __forceinline__ void store_moment8(void *base, uint64_t e, const floa
     }
 }
 
-template <int W, int CAP, int VPT, bool MV16>
-__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThreads, 1)
+template <int W, int CAP, int CTAS, int THREADS, int VPT, bool MV16>
+__global__ void __launch_bounds__(THREADS, 1)
 zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
 {
-    constexpr int kWarps = kSmallThreads / 32;
-    constexpr uint32_t kStride = kSmallCtas * kSmallThreads;
+    constexpr int kWarps = THREADS / 32;
+    constexpr uint32_t kStride = CTAS * THREADS;
     __shared__ double red_a[kWarps], red_b[kWarps];
     __shared__ double part[2];
     __shared__ float clip;
     __shared__ StepScalars ssc;
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
-    const uint32_t gt = blockIdx.x * kSmallThreads + threadIdx.x;
+    const uint32_t gt = blockIdx.x * THREADS + threadIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Capturable: this step is t + 1; every CTA reads t here, before the
     // first cluster barrier, and CTA 0 advances it after the second.
@@ -836,18 +836,19 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
         part[0] = x;
         part[1] = y;
     }
+    static_assert(CTAS > 1 && CTAS <= 32, "a cluster of 2..32 CTAs (one lane per CTA below)");
     cluster_sync();            // every CTA's partials are written
     if (warp == 0) {
         // Lane r fetches CTA r's pair (one remote round trip for all), then
         // lane 0 adds them in rank order.
         double pa = 0.0, pb = 0.0;
-        if (lane < kSmallCtas) {
+        if (lane < CTAS) {
             pa = ld_cluster_f64(&part[0], (uint32_t)lane);
             pb = ld_cluster_f64(&part[1], (uint32_t)lane);
         }
         double x = 0.0, y = 0.0;
 #pragma unroll
-        for (int r = 0; r < kSmallCtas; ++r) {
+        for (int r = 0; r < CTAS; ++r) {
             x += __shfl_sync(0xFFFFFFFFu, pa, r);
             y += __shfl_sync(0xFFFFFFFFu, pb, r);
         }
@@ -900,7 +901,7 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes)
     return allow_dynamic_smem(reinterpret_cast<const void *>(kernel), (int)bytes);
 }
 
-template <int W, int CAP, int VPT, bool MV16>
+template <int W, int CAP, int CTAS, int THREADS, int VPT, bool MV16>
 cudaError_t launch_small_v(const StepLaunch &s, cudaStream_t stream)
 {
     SmallParams<CAP> sp{};
@@ -920,20 +921,34 @@ cudaError_t launch_small_v(const StepLaunch &s, cudaStream_t stream)
     sp.max_norm = s.max_norm;
     sp.clip_eps = s.clip_eps;
     sp.dev = s.dev;
-    zero1_small_step_kernel<W, CAP, VPT, MV16><<<kSmallCtas, kSmallThreads, 0, stream>>>(sp);
-    return cudaGetLastError();
+    // One thread-block cluster of CTAS CTAs (distributed shared memory and
+    // the cluster barrier need them co-scheduled).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CTAS, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, zero1_small_step_kernel<W, CAP, CTAS, THREADS, VPT, MV16>, sp);
 }
 
 template <int W, int CAP>
 cudaError_t launch_small(const StepLaunch &s, cudaStream_t stream)
 {
+    constexpr int C = kSmallCtas, T = kSmallThreads;
     switch (s.small_vpt * 2 + (s.moments_bf16 ? 1 : 0)) {
-    case 2: return launch_small_v<W, CAP, 1, false>(s, stream);
-    case 3: return launch_small_v<W, CAP, 1, true>(s, stream);
-    case 4: return launch_small_v<W, CAP, 2, false>(s, stream);
-    case 5: return launch_small_v<W, CAP, 2, true>(s, stream);
-    case 8: return launch_small_v<W, CAP, 4, false>(s, stream);
-    case 9: return launch_small_v<W, CAP, 4, true>(s, stream);
+    case 2: return launch_small_v<W, CAP, C, T, 1, false>(s, stream);
+    case 3: return launch_small_v<W, CAP, C, T, 1, true>(s, stream);
+    case 4: return launch_small_v<W, CAP, C, T, 2, false>(s, stream);
+    case 5: return launch_small_v<W, CAP, C, T, 2, true>(s, stream);
+    case 8: return launch_small_v<W, CAP, C, T, 4, false>(s, stream);
+    case 9: return launch_small_v<W, CAP, C, T, 4, true>(s, stream);
     default: return cudaErrorInvalidValue;
     }
 }
