@@ -97,3 +97,89 @@ def test_unknown_handles_are_rejected_not_dereferenced(lib_path):
         assert e.value.code == -1
     z.zero1_destroy(None)                      # NULL is accepted
     assert "invalid handle" in z.zero1_last_error() or z.zero1_last_error() == ""
+
+
+def _declarations() -> dict[str, list[str]]:
+    """Each declared entry point's parameter list, from include/zero1.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(zero1_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M | re.S):
+        params = [p.strip() for p in m.group(2).replace("\n", " ").split(",")]
+        out[m.group(1)] = [] if params == ["void"] or params == [""] else params
+    return out
+
+
+def test_binding_signatures_match_header():
+    """The ctypes binding passes as many arguments as each C prototype takes,
+    and pointer parameters are marshalled as pointers."""
+    decls = _declarations()
+    assert set(decls) == set(z.EXPORTED_SYMBOLS)
+    for name, params in decls.items():
+        _, args = z._SIGS[name]
+        assert len(args) == len(params), (name, params, args)
+        for p, a in zip(params, args):
+            if "*" in p:
+                assert a is C.c_void_p, (name, p)
+
+
+def _struct_fields(name: str) -> list[tuple[str, str]]:
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct(?: \w+)? \{([^}]*)\}\s*" + name + r";", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        ctype, names = decl.split(None, 1)
+        fields += [(n.strip(), ctype) for n in names.split(",")]
+    return fields
+
+
+CTYPES = {"double": C.c_double, "uint32_t": C.c_uint32, "int32_t": C.c_int32}
+
+
+@pytest.mark.parametrize("struct,binding", [("zero1_options", z._COptions), ("zero1_hparams", z._CHparams)])
+def test_structs_match_header(struct, binding):
+    fields = _struct_fields(struct)
+    assert [n for n, _ in fields] == [n for n, _ in binding._fields_]
+    for (n, ctype), (_, bt) in zip(fields, binding._fields_):
+        assert CTYPES[ctype] is bt, (struct, n, ctype, bt)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_options_checked_before_the_device(lib_path):
+    """Valid options pass the checks (the call then finds no device); a wrong
+    size or an out-of-range field is rejected first."""
+    with pytest.raises(z.Zero1Error) as e:
+        z.zero1_create_ex(4096, 4, None, z.Options(capturable=True, small_step=-1, moments_bf16=True))
+    assert e.value.code == -5
+    lib = z._load()
+    hp = z.Hparams()._c()
+    h = C.c_void_p()
+    for field, value in (("size", 8), ("small_step", 2), ("capturable", 3), ("bucket_ctas", -1), ("clip_eps", -1.0)):
+        opts = z.Options()._c()
+        setattr(opts, field, value)
+        assert lib.zero1_create_ex(4096, 4, C.byref(hp), C.byref(opts), C.byref(h)) == -1, field
+
+
+def test_new_entry_points_reject_unknown_handles(lib_path):
+    bogus = 0xDEAD0000
+    for call in (lambda: z.zero1_step_host_async(bogus, [16], [16]),
+                 lambda: z.zero1_host_sync(bogus),
+                 lambda: z.zero1_profile_read(bogus, 4),
+                 lambda: z.zero1_step_launches(bogus),
+                 lambda: z.zero1_set_lr_ptr(bogus, 16),
+                 lambda: z.zero1_bucket_begin(bogus)):
+        with pytest.raises(z.Zero1Error) as e:
+            call()
+        assert e.value.code == -1
+
+
+def test_ptr_table_marshals_once():
+    bufs = [torch.zeros(4), torch.zeros(4)]
+    t = z.PtrTable(bufs)
+    assert len(t) == 2
+    assert [t.array[i] for i in range(2)] == [b.data_ptr() for b in bufs]
+    assert z._ptrs(t) is t.array
+    assert list(z._ptrs([16, None])) == [16, None]
