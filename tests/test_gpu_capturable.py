@@ -122,6 +122,50 @@ def test_graph_replay(n, world):
     assert all(np.array_equal(u16(a), u16(b)) for a, b in zip(reps, reps_ref))
 
 
+@pytest.mark.parametrize("n,world", [(100_003, 8), (4099, 4)])
+@pytest.mark.parametrize("variant", ["bf16_moments", "decay_first_clip_eps"])
+def test_graph_replay_variants(n, world, variant):
+    """The step variants replayed from a CUDA graph equal plain steps."""
+    kw = ({"moments_bf16": True} if variant == "bf16_moments"
+          else {"decay_before_update": True, "clip_eps": 1e-6})
+    w = WL.Workload("gv", n, world, 0.01, 5, lr=1e-2, weight_decay=0.3, max_norm=0.05)
+    hp = z.Hparams(**w.hparams())
+    m0 = WL.master(w, "cuda")
+    dt = torch.bfloat16 if kw.get("moments_bf16") else torch.float32
+
+    def state(opt):
+        master = torch.empty(n, dtype=torch.float32, device="cuda")
+        m, v = torch.empty(n, dtype=dt, device="cuda"), torch.empty(n, dtype=dt, device="cuda")
+        t = opt.get_state(master, m, v)
+        torch.cuda.synchronize()
+        return [x.view(torch.int32 if x.dtype == torch.float32 else torch.int16).cpu() for x in (master, m, v)], t
+
+    reps_ref = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world, hp, z.Options(**kw)) as ref:
+        ref.set_state(m0)
+        for t in range(1, 6):
+            ref.step(WL.grads(w, t, "cuda"), reps_ref)
+        want = state(ref)
+    grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    reps = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world, hp, z.Options(capturable=True, **kw)) as opt:
+        opt.set_state(m0)
+        WL.grads(w, 1, "cuda", out=grads)
+        opt.step(grads, reps, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            opt.step(grads, reps, torch.cuda.current_stream())
+        for t in range(2, 6):
+            WL.grads(w, t, "cuda", out=grads)
+            g.replay()
+        torch.cuda.synchronize()
+        got = state(opt)
+    assert got[1] == want[1] == 5
+    assert all(torch.equal(a, b) for a, b in zip(got[0], want[0]))
+    assert all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(reps, reps_ref))
+
+
 def test_capturable_bucketed_equals_plain():
     n, world = 200_003, 8
     w = WL.Workload("bk", n, world, 0.01, 3, max_norm=0.05)

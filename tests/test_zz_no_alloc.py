@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-6
 
 
-@pytest.mark.parametrize("n,world", [(1_000_003, 8), (65_541, 2)])
+@pytest.mark.parametrize("n,world", [(1_000_003, 8), (65_541, 2), (4099, 4)])   # two kernels, re-read, one launch
 def test_noalloc_matches_handle_step_on_two_calls(n, world):
     w = WL.Workload(f"noalloc_{n}_{world}", n, world, 0.02, 2, max_norm=0.5)
     hp = z.Hparams(**w.hparams())
