@@ -37,7 +37,7 @@ def _same(a, b):
         assert bits_equal(x, y)
 
 
-SHAPES = [(100_003, 8), (4099, 4), (4096, 4), (70_001, 2)]   # two kernels (W >= 3, W <= 2), the one-launch cluster and one-CTA paths
+SHAPES = [(100_003, 8), (4099, 4), (4096, 4), (70_001, 2)]   # two kernels (W >= 3), the one-launch cluster (ragged and 8-aligned), re-read (W <= 2)
 
 
 @pytest.mark.parametrize("n,world", SHAPES)
