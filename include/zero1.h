@@ -128,6 +128,11 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     (for schedules inside a graph); zero1_get_state reads t from the
  *     device; zero1_set_state writes it.  Profiling (zero1_profile_start)
  *     must not be active while a step is being captured.
+ *   inject_wait_timeout: failure testing only.  1 = the update kernel's
+ *     producer issues no loads, so every pipeline wait of that kernel runs
+ *     out after its 1 s limit; the step returns without hanging, and
+ *     zero1_get_grad_norm then reports ZERO1_ECUDA (the sticky timeout bit).
+ *     Applies to the two-kernel path (set small_step = -1 for small n).
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -137,6 +142,7 @@ typedef struct zero1_options {
     int32_t bucket_ctas;
     int32_t small_step;
     int32_t capturable;
+    int32_t inject_wait_timeout;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).

@@ -95,7 +95,7 @@ class Hparams:
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
                 ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32),
-                ("capturable", C.c_int32)]
+                ("capturable", C.c_int32), ("inject_wait_timeout", C.c_int32)]
 
 
 @dataclass
@@ -110,11 +110,12 @@ class Options:
     bucket_ctas: int = 0
     small_step: int = 0
     capturable: bool = False
+    inject_wait_timeout: bool = False    # failure testing: the update kernel's waits run out
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
                          1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step,
-                         1 if self.capturable else 0)
+                         1 if self.capturable else 0, 1 if self.inject_wait_timeout else 0)
 
 
 _lib = None

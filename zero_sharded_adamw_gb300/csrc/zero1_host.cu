@@ -261,6 +261,8 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         if (opts->bucket_ctas < 0) return fail(ZERO1_EINVAL, "bucket_ctas must be >= 0");
         if (opts->small_step < -1 || opts->small_step > 1) return fail(ZERO1_EINVAL, "small_step must be -1, 0 or 1");
         if (opts->capturable != 0 && opts->capturable != 1) return fail(ZERO1_EINVAL, "capturable must be 0 or 1");
+        if (opts->inject_wait_timeout != 0 && opts->inject_wait_timeout != 1)
+            return fail(ZERO1_EINVAL, "inject_wait_timeout must be 0 or 1");
         o = *opts;
     }
 
@@ -394,6 +396,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.clip_eps = h->opts.clip_eps;
     s.small_vpt = zero1::small_step_vpt(h->n, h->world, h->opts.small_step);
     s.dev = dev_scalars(h);
+    s.stall_test = h->opts.inject_wait_timeout != 0;
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);

@@ -119,6 +119,7 @@ struct UpdParams {
     int nbuckets;
     double max_norm, clip_eps;
     DevScalars dev;              // capturable: scalars formed from the device step counter
+    int stall_test;              // failure test: the producer issues nothing, so every wait runs out
 };
 
 // Scalar rank-ordered sum for the last n % 8 parameters.
@@ -569,7 +570,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     const uint64_t once = policy_evict_first();
 
     if (warp == kUpdConsumerWarps) {                              // producer
-        if (lane == 0) {
+        if (lane == 0 && !p.stall_test) {
             uint32_t k = 0;
             for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
                 const int s = k % kUpdStages;
@@ -999,6 +1000,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     up.max_norm = s.max_norm;
     up.clip_eps = s.clip_eps;
     up.dev = s.dev;
+    up.stall_test = s.stall_test ? 1 : 0;
 
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
