@@ -49,6 +49,13 @@ namespace {
 using namespace ptx;
 
 constexpr int kTile = 2048;                      // parameters per tile
+// 1: whole steps launch their two kernels with programmatic dependencies
+// (programmatic dependent launch).  Off by default: measured in 50-step CUDA
+// graphs on GB300 it was mixed -- 7% faster at 65,536 parameters (W = 4),
+// 0.1% at 124M (W = 8), but 3% slower at 1M and 2% at 4M (W = 8).
+#ifndef ZERO1_PDL
+#define ZERO1_PDL 0
+#endif
 constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel (3 and 2 measured slower)
 // The update kernel's ring depth and consumer warps, per path (measured on
 // GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment workloads): with an
@@ -273,6 +280,12 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // Launched with a programmatic dependency (whole steps without
+    // profiling events): the update kernel may launch now; this kernel reads
+    // nothing (the gradients may come from the kernel before it) until the
+    // previous grid has completed.
+    launch_dependents();
+    grid_dependency_wait();
 
     if (warp == kConsumerWarps) {                                 // producer
         if (lane == 0) {
@@ -529,6 +542,12 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     const int64_t first = ntiles - 1 - (int64_t)blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
+
+    // Programmatic dependency on the reduce-scatter kernel: the next step's
+    // kernel may launch now; ĝ and the clip coefficient are read only after
+    // the reduce-scatter grid has completed.
+    launch_dependents();
+    grid_dependency_wait();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kUpdStages; ++s) {
@@ -1017,16 +1036,29 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     const size_t k2_smem = path == 1 ? sizeof(UpdSmem<S1>) : path == 2 ? sizeof(UpdSmem<S2>) : sizeof(UpdSmem<S0>);
     const int k2_threads = (path == 1 ? C1 : path == 2 ? C2 : C0) * 32 + 64;
     if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
+    // A whole step without profiling events between its kernels launches
+    // both with a programmatic dependency on the kernel before them in the
+    // stream: each may launch while its predecessor drains and waits for it
+    // in grid_dependency_wait before touching memory.
+    const bool pdl = ZERO1_PDL && !ev && s.phase == 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c1 = {};
+    c1.gridDim = dim3(s.grid_rs);
+    c1.blockDim = dim3(kRsThreads);
+    c1.dynamicSmemBytes = sizeof(RsSmem);
+    c1.stream = stream;
+    c1.attrs = attr;
+    c1.numAttrs = pdl ? 1 : 0;
+    cudaLaunchConfig_t c2 = c1;
+    c2.gridDim = dim3(s.grid_update);
+    c2.blockDim = dim3(k2_threads);
+    c2.dynamicSmemBytes = k2_smem;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    if (s.phase != 2) {
-        k1<<<s.grid_rs, kRsThreads, sizeof(RsSmem), stream>>>(rp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (s.phase != 2 && (e = cudaLaunchKernelEx(&c1, k1, rp)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
-    if (s.phase != 1) {
-        k2<<<s.grid_update, k2_threads, k2_smem, stream>>>(up);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (s.phase != 1 && (e = cudaLaunchKernelEx(&c2, k2, up)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }

@@ -163,6 +163,17 @@ __device__ __forceinline__ void drain_loads(uint64_t *full, uint32_t issued)
     }
 }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Let the next kernel of the stream launch now, if it was launched with a
+// programmatic dependency on this one (it still waits for this grid in its
+// own grid_dependency_wait).  No-op otherwise.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Wait until the grid this one programmatically depends on has completed
+// and its memory is visible.  No-op for a launch without that dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------ thread-block cluster
 
 // All threads of all CTAs of the cluster arrive and wait (the non-.aligned
