@@ -2,7 +2,7 @@
 
 A thin ctypes binding of ``libzero1.so`` (C ABI in ``include/zero1.h``): the
 functions below carry the C entry points' names and only marshal arguments.
-Every step of the path runs in the library's two CUDA kernels; there is no
+Every step of the path runs in the library's CUDA kernels; there is no
 CPU fallback.  The library is built by ``__graft_entry__.build()`` (or
 ``python -m zero_sharded_adamw_gb300._build``); calling any entry point
 without it raises ``Zero1Error``.
