@@ -705,7 +705,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 
 // Small steps: the whole step in one launch of one thread-block cluster.
 // Each thread owns up to VPT 8-parameter vectors (vector i of thread g of
-// the cluster is g + i * kSmallCtas * kSmallThreads).  It loads their
+// the cluster is g + i * kSmallCtas * kSmallThreads, threads numbered with
+// the warps interleaved over the CTAs).  It loads their
 // master, m, v and their W gradients (in batches of loads issued before
 // any add), forms the rank-ordered mean and its squares, and keeps both in
 // registers; the CTAs' fixed-order partial sums meet through distributed
@@ -766,7 +767,10 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
     __shared__ StepScalars ssc;
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
-    const uint32_t gt = blockIdx.x * THREADS + threadIdx.x;
+    // Warps are dealt round-robin over the CTAs (warp i of CTA b is global
+    // warp i * CTAS + b), so even a few vectors' worth of work spreads over
+    // every SM of the cluster; each warp still covers 32 consecutive vectors.
+    const uint32_t gt = ((threadIdx.x >> 5) * CTAS + blockIdx.x) * 32u + (threadIdx.x & 31u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Capturable: this step is t + 1; every CTA reads t here, before the
     // first cluster barrier, and CTA 0 advances it after the second.
