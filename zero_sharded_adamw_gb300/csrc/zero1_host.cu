@@ -20,6 +20,7 @@
 #include <mutex>
 #include <new>
 #include <set>
+#include <tuple>
 #include <unordered_set>
 #include <algorithm>
 #include <utility>
@@ -182,23 +183,29 @@ void zero1::set_error_message(const char *msg)
     snprintf(g_err, sizeof g_err, "%s", msg);
 }
 
-cudaError_t zero1::allow_dynamic_smem(const void *kernel, int bytes)
+cudaError_t zero1::set_func_attribute_once(const void *kernel, cudaFuncAttribute attr, int value)
 {
     static std::mutex mu;
-    static std::set<std::pair<const void *, int>> done;
+    static std::set<std::tuple<const void *, int, int>> done;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(kernel, dev, (int)attr);
     {
         std::lock_guard<std::mutex> lk(mu);
-        if (done.count({kernel, dev})) return cudaSuccess;
+        if (done.count(key)) return cudaSuccess;
     }
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(kernel, attr, value);
     if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lk(mu);
-        done.insert({kernel, dev});
+        done.insert(key);
     }
     return e;
+}
+
+cudaError_t zero1::allow_dynamic_smem(const void *kernel, int bytes)
+{
+    return set_func_attribute_once(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 extern "C" {

@@ -86,8 +86,12 @@ struct StepLaunch {
 
 // The one-launch path for small n: a cluster of kSmallCtas CTAs of
 // kSmallThreads threads, each thread holding up to kSmallMaxVpt vectors.
-constexpr int kSmallCtas = 8;
-constexpr int kSmallThreads = 256;
+#ifndef ZERO1_SMALL_CTAS
+#define ZERO1_SMALL_CTAS 8
+#define ZERO1_SMALL_THREADS 256
+#endif
+constexpr int kSmallCtas = ZERO1_SMALL_CTAS;        // 8 is the portable cluster maximum
+constexpr int kSmallThreads = ZERO1_SMALL_THREADS;
 constexpr int kSmallMaxVpt = 4;
 constexpr uint64_t kSmallCap = (uint64_t)kSmallCtas * kSmallThreads * kVec * kSmallMaxVpt;   // 65,536
 
@@ -113,6 +117,8 @@ cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *e
 // call keeps a step's host path short and free of non-stream calls (so a
 // step can be captured in a CUDA graph after one uncaptured step).
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
+// The same once-per-(kernel, device, attribute) rule for any function attribute.
+cudaError_t set_func_attribute_once(const void *kernel, cudaFuncAttribute attr, int value);
 
 // Grid sizes: one wave of resident CTAs on this device, capped by the work.
 void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);

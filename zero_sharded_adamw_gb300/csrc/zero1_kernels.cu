@@ -959,7 +959,13 @@ cudaError_t launch_small_v(const StepLaunch &s, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, zero1_small_step_kernel<W, CAP, CTAS, THREADS, VPT, MV16>, sp);
+    auto kern = zero1_small_step_kernel<W, CAP, CTAS, THREADS, VPT, MV16>;
+    if (CTAS > 8) {   // past the portable cluster size
+        cudaError_t e = set_func_attribute_once(reinterpret_cast<const void *>(kern),
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
 template <int W, int CAP>
