@@ -185,10 +185,11 @@ def test_bf16_master_example():
 
 # --------------------------------------------------- semantics and errors
 
-def test_checkpoint_resume_is_exact():
+@pytest.mark.parametrize("n", [30_011, 300_007])      # one-launch and two-kernel path
+def test_checkpoint_resume_is_exact(n):
     """10 steps == 5 steps, save (per-rank shard ranges, to host), destroy,
     create, load, 5 steps -- bit for bit ("a checkpoint carries m, v, t")."""
-    w = WL.Workload("ckpt", 30_011, 4, 0.01, 10, max_norm=0.05)
+    w = WL.Workload("ckpt", n, 4, 0.01, 10, max_norm=0.05)
     zhp, _ = _hp(w)
     m0 = WL.master(w, "cuda")
     grads = [torch.empty(w.n, dtype=torch.bfloat16, device="cuda") for _ in range(w.world)]
@@ -240,17 +241,19 @@ def test_deterministic():
     assert np.array_equal(r1, r2)
 
 
+@pytest.mark.parametrize("small_step", [1, -1])
 @pytest.mark.parametrize("bad", ["inf", "nan"])
-def test_nonfinite_gradient_propagates(bad):
+def test_nonfinite_gradient_propagates(bad, small_step):
     """An inf or NaN in one rank's gradient: the norm is not finite and the
-    state follows the oracle's IEEE propagation (NaN positions match)."""
+    state follows the oracle's IEEE propagation (NaN positions match), on
+    the one-launch and the two-kernel path."""
     w = WL.Workload("nf", 4099, 4, 0.01, 1)
     zhp, ohp = _hp(w)
     grads = WL.grads(w, 1, "cuda")
     grads[2][17] = float(bad)
     reps = [torch.empty_like(grads[0]) for _ in range(w.world)]
     m0 = WL.master(w, "cuda")
-    with z.Zero1(w.n, w.world, zhp) as opt:
+    with z.Zero1(w.n, w.world, zhp, z.Options(small_step=small_step)) as opt:
         opt.set_state(m0)
         opt.step(grads, reps)
         norm, c = opt.grad_norm()
@@ -285,9 +288,12 @@ def test_argument_errors():
     assert e.value.code == -1
 
 
-def test_max_world():
+@pytest.mark.parametrize("small_step", [1, -1])
+def test_max_world(small_step):
+    """W = 512 (the runtime-W kernels with the largest pointer tables) on the
+    one-launch and the two-kernel path."""
     w = WL.Workload("wmax", 1003, z.ZERO1_MAX_WORLD, 0.01, 2, max_norm=0.5)
-    run_parity(w, 2)
+    run_parity(w, 2, opts=z.Options(small_step=small_step), launches=1 if small_step == 1 else 2)
 
 
 def test_layout_and_footprint():
