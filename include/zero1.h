@@ -147,7 +147,10 @@ typedef struct zero1_options {
 
 /* zero1_create with step variants (opts may be NULL: the default step).
  * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
- * negative or non-finite clip_eps, a negative bucket_ctas. */
+ * negative or non-finite clip_eps, a negative bucket_ctas, small_step
+ * outside {-1, 0, 1}, capturable or inject_wait_timeout outside {0, 1}, and
+ * a capturable handle whose bias corrections would need more than 2^22
+ * table entries.  All option checks come before any device call. */
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
                     zero1_handle *out);
 
@@ -233,14 +236,17 @@ int zero1_host_sync(zero1_handle h);
  * v fp32, or bf16 for a handle created with moments_bf16; m or v may be
  * NULL, meaning zeros.  t: the number of steps already taken (the next step
  * uses t+1).  Enqueued on `stream`; a pageable host source is consumed
- * before the call returns.  Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
+ * before the call returns.  On a capturable handle t is also written to the
+ * device counter, and the call waits for `stream`.
+ * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
 int zero1_set_state(zero1_handle h, const float *master, const void *m, const void *v,
                     uint64_t t, void *stream);
 
 /* Checkpoint save: copies master, m, v (n fp32 each) into device or host
  * arrays (any may be NULL to skip it) and writes the step count to *t (may
  * be NULL).  Enqueued on `stream`; synchronize it before reading a host
- * destination. */
+ * destination.  On a capturable handle t is read from the device counter
+ * (replayed graphs advance it), which waits for `stream`. */
 int zero1_get_state(zero1_handle h, float *master, void *m, void *v, uint64_t *t, void *stream);
 
 /* The same two copies for parameters [offset, offset+count) only -- one
@@ -253,8 +259,11 @@ int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float
                           void *m, void *v, void *stream);
 
 /* Change the learning rate used by later steps (schedules such as warmup +
- * cosine, "Parallel training", "training loop and checkpoint").
- * Errors: ZERO1_EINVAL for a NULL handle or lr < 0 or not finite. */
+ * cosine, "Parallel training", "training loop and checkpoint").  On a
+ * capturable handle it writes the handle's device lr slot after waiting for
+ * the whole device (steps already enqueued keep the old rate).
+ * Errors: ZERO1_EINVAL for a NULL handle or lr < 0 or not finite,
+ * ZERO1_ECUDA. */
 int zero1_set_lr(zero1_handle h, double lr);
 
 /* Capturable handles only: later steps (and replays of captured steps)
@@ -285,8 +294,10 @@ int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint
  * all-gather kernel).  zero1_profile_stop waits for the last recorded event
  * and returns the summed kernel times in milliseconds and the number of
  * steps recorded; it frees the events.  Either kernel's average launch
- * duration is its sum divided by *steps.  Outputs may be NULL.
- * Errors: ZERO1_EINVAL (capacity < 1, or stop without start), ZERO1_ECUDA. */
+ * duration is its sum divided by *steps.  On the one-launch path the first
+ * interval is the whole kernel and the second is empty.  Outputs may be
+ * NULL.  Errors: ZERO1_EINVAL (capacity < 1, or stop without start),
+ * ZERO1_ECUDA. */
 int zero1_profile_start(zero1_handle h, int capacity);
 int zero1_profile_stop(zero1_handle h, double *rs_norm_ms, double *update_ms, uint64_t *steps);
 
