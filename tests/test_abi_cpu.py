@@ -184,3 +184,14 @@ def test_ptr_table_marshals_once():
     assert [t.array[i] for i in range(2)] == [b.data_ptr() for b in bufs]
     assert z._ptrs(t) is t.array
     assert list(z._ptrs([16, None])) == [16, None]
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the built library every entry point raises (no CPU fallback)."""
+    monkeypatch.setattr(z, "_LIB_PATH", str(tmp_path / "libzero1.so"))
+    monkeypatch.setattr(z, "_lib", None)
+    for call in (lambda: z.zero1_create(4096, 4), lambda: z.zero1_shard_plan(10, 2),
+                 lambda: z.Zero1(16, 2), lambda: z.zero1_last_error()):
+        with pytest.raises(z.Zero1Error) as e:
+            call()
+        assert e.value.code == -5 and "not built" in str(e.value)
