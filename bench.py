@@ -487,15 +487,20 @@ def zero2_arm(args, w: WL.Workload):
     first), the two GEMMs a layer's backward runs on T tokens (2*T*P flops
     each, bf16 on cuBLAS) on a compute stream; each bucket is handed to
     zero1_bucket_reduce on a second stream as soon as its GEMMs finish, and
-    zero1_bucket_finish runs after the backward.  Reported: the backward
-    alone, backward + zero1_step back to back (the ZeRO-1 schedule), and the
-    overlapped schedule; the optimizer time left exposed after the backward
-    is the figure of merit."""
+    zero1_bucket_finish runs after the backward.  With --bucket-update
+    (clipping off in every schedule) each bucket is reduced and updated at
+    once by zero1_bucket_update.  Reported: the backward alone, backward +
+    zero1_step back to back (the ZeRO-1 schedule), and the overlapped
+    schedule; the optimizer time left exposed after the backward is the
+    figure of merit."""
     import zero_sharded_adamw_gb300 as z
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    hp = z.Hparams(**w.hparams())
+    hpd = w.hparams()
+    if args.bucket_update:
+        hpd["max_norm"] = 0.0                   # an update per bucket needs no global norm
+    hp = z.Hparams(**hpd)
     grads = WL.grads(w, 1, dev)
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     per_bucket = max(8, (int(args.bucket_mb * 1e6) // 2) // 8 * 8)
@@ -534,9 +539,13 @@ def zero2_arm(args, w: WL.Workload):
             z.zero1_bucket_begin(opt.handle)
             for off, cnt, ev in evs:
                 comm.wait_event(ev)
-                z.zero1_bucket_reduce(opt.handle, off, cnt, [g[off:off + cnt] for g in grads], comm)
+                if args.bucket_update:
+                    z.zero1_bucket_update(opt.handle, off, cnt, [g[off:off + cnt] for g in grads],
+                                          [r[off:off + cnt] for r in reps], comm)
+                else:
+                    z.zero1_bucket_reduce(opt.handle, off, cnt, [g[off:off + cnt] for g in grads], comm)
             main.wait_stream(comm)
-            z.zero1_bucket_finish(opt.handle, reps, main)
+            z.zero1_bucket_finish(opt.handle, None if args.bucket_update else reps, main)
 
     # Blackwell cuBLAS GEMMs are persistent and hold every SM until they end,
     # so a backward leaves room for concurrent bucket reduces only if its
@@ -570,6 +579,7 @@ def zero2_arm(args, w: WL.Workload):
         "config": {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world, "buckets": len(cuts),
                    "bucket_params": per_bucket, "tokens": args.tokens, "bucket_ctas": args.bucket_ctas,
                    "gemm_sm_carveout": carveout, "backward": args.backward,
+                   "bucket_update": args.bucket_update, "max_norm": hpd["max_norm"],
                    "sleep_us_per_bucket": args.sleep_us if args.backward == "sleep" else None},
         "ms": {"backward_alone": out["bwd"], "backward_then_step": out["seq"], "overlapped": out["overlap"]},
         "exposed_ms": {"zero1_schedule": out["seq"] - out["bwd"], "zero2_overlapped": out["overlap"] - out["bwd"]},
@@ -697,6 +707,8 @@ def main(argv=None):
     ap.add_argument("--bucket-mb", type=float, default=25.0, help="zero2: bucket size per rank (MB of bf16)")
     ap.add_argument("--tokens", type=int, default=8192, help="zero2: tokens of the emulated backward")
     ap.add_argument("--bucket-ctas", type=int, default=32, help="zero2: CTAs per bucket reduce (0 = one per SM)")
+    ap.add_argument("--bucket-update", action="store_true",
+                    help="zero2: clipping off; reduce and update each bucket at once (zero1_bucket_update)")
     ap.add_argument("--backward", default="gemm", choices=["gemm", "sleep"],
                     help="zero2: emulated backward: bf16 GEMMs, or a one-SM latency-bound kernel per bucket")
     ap.add_argument("--sleep-us", type=float, default=240.0, help="zero2: sleep backward, microseconds per bucket")

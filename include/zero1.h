@@ -201,17 +201,33 @@ int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *
  *     partial.  The gradient buffers may be reused once `stream` passes the
  *     call.  Issue all of one step's buckets on one stream (they share
  *     per-launch scratch); that stream may run alongside the caller's
- *     backward on another.  At most 4096 buckets, in any order.
+ *     backward on another.  At most 4096 buckets, in any order; they may
+ *     not overlap, and only the bucket that ends at n may have a count that
+ *     is not a multiple of 8.
+ *   zero1_bucket_update(h, offset, count, grad_ptrs, param_ptrs, stream):
+ *     for handles without clipping (max_norm <= 0), where no step of the
+ *     update waits for the global norm: the bucket's reduce-scatter and,
+ *     right after it, the AdamW + bf16 + all-gather of the bucket's own
+ *     parameters.  param_ptrs[r] points at rank r's replica for exactly
+ *     that range.  So the whole optimizer step runs beside the backward.
+ *     One step uses zero1_bucket_reduce or zero1_bucket_update, not both;
+ *     not available on capturable handles.
  *   zero1_bucket_finish(h, param_ptrs, stream): the buckets must cover
- *     [0, n) exactly once (else ZERO1_EINVAL and the step is abandoned);
- *     forms the norm from the buckets' partials in call order, clips, runs
- *     the AdamW + bf16 + all-gather kernel over all n, t -> t+1.
+ *     [0, n) exactly once (else ZERO1_EINVAL and the step is abandoned;
+ *     buckets already updated by zero1_bucket_update stay updated); forms
+ *     the norm from the buckets' partials in call order, clips, runs the
+ *     AdamW + bf16 + all-gather kernel over all n, t -> t+1.  After
+ *     zero1_bucket_update buckets it launches nothing (param_ptrs may be
+ *     NULL) and only advances t; the norm was recorded with the last
+ *     bucket.
  * The result equals zero1_step's for the same clip coefficient bit for bit;
  * the norm itself is summed in a bucketing-dependent (but fixed) order.
  * zero1_step is refused while a bucketed step is open. */
 int zero1_bucket_begin(zero1_handle h);
 int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs,
                         void *stream);
+int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs,
+                        void *const *param_ptrs, void *stream);
 int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream);
 
 /* The host-buffer step, pipelined: enqueue and return.  Uploads this step's

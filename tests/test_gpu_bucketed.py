@@ -154,3 +154,75 @@ def test_bucket_errors():
         z.zero1_bucket_finish(opt.handle, g)
         torch.cuda.synchronize()
         assert opt.get_state() == 1
+
+
+def _bucketed_update_step(opt: z.Zero1, grads, reps, cuts, side: torch.cuda.Stream):
+    """zero1_bucket_update per bucket on a side stream (clipping off), then
+    zero1_bucket_finish with no replica pointers."""
+    z.zero1_bucket_begin(opt.handle)
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    keep = []
+    with torch.cuda.stream(side):
+        for off, cnt in cuts:
+            bucket = [g[off:off + cnt].clone() for g in grads]
+            keep.append(bucket)
+            z.zero1_bucket_update(opt.handle, off, cnt, bucket, [r[off:off + cnt] for r in reps], side)
+    main.wait_stream(side)
+    z.zero1_bucket_finish(opt.handle, None, main)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("n,world,mean", [(777_777, 8, 3000), (65_541, 2, 300), (4099, 4, 37)])
+def test_bucket_update_equals_plain_step_without_clipping(n, world, mean):
+    """Without clipping each bucket is updated right after its reduce-scatter;
+    the result equals zero1_step's bit for bit, the norm within 1e-6."""
+    w = WL.Workload("upd", n, world, 0.02, 3, max_norm=0.0)
+    hp = z.Hparams(**w.hparams())
+    rng = np.random.default_rng(n)
+    side = torch.cuda.Stream()
+    m0 = WL.master(w, "cuda")
+    ra = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    rb = [torch.empty_like(ra[0]) for _ in range(world)]
+    with z.Zero1(n, world, hp, z.Options(small_step=-1)) as a, z.Zero1(n, world, hp) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, 4):
+            grads = WL.grads(w, t, "cuda")
+            a.step(grads, ra)
+            _bucketed_update_step(b, grads, rb, _buckets(n, rng, mean), side)
+            na, ca = a.grad_norm()
+            nb, cb = b.grad_norm()
+            assert ca == cb == 1.0 and abs(na - nb) <= 1e-6 * na
+        assert a.get_state() == b.get_state() == 3
+        for x, y in zip(_state(a, n), _state(b, n)):
+            assert bits_equal(x, y)
+        assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+
+
+def test_bucket_update_errors():
+    n, world = 1000, 2
+    g = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    r = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world) as opt:                                # clipping on (max_norm 1.0)
+        z.zero1_bucket_begin(opt.handle)
+        with pytest.raises(z.Zero1Error) as e:
+            z.zero1_bucket_update(opt.handle, 0, n, g, r)
+        assert "clipping off" in str(e.value)
+    with z.Zero1(n, world, z.Hparams(max_norm=0.0), z.Options(capturable=True)) as opt:
+        z.zero1_bucket_begin(opt.handle)
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_update(opt.handle, 0, n, g, r)
+    with z.Zero1(n, world, z.Hparams(max_norm=0.0)) as opt:
+        z.zero1_bucket_begin(opt.handle)
+        z.zero1_bucket_update(opt.handle, 0, 496, g, r)
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_reduce(opt.handle, 496, 504, [x[496:] for x in g])    # mixing the two kinds
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_update(opt.handle, 488, 16, [x[488:] for x in g], [x[488:] for x in r])   # overlap
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bucket_update(opt.handle, 496, 13, [x[496:] for x in g], [x[496:] for x in r])   # ragged mid-way
+        z.zero1_bucket_update(opt.handle, 496, 504, [x[496:] for x in g], [x[496:] for x in r])
+        z.zero1_bucket_finish(opt.handle, None)
+        torch.cuda.synchronize()
+        assert opt.get_state() == 1

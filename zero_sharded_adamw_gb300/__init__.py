@@ -23,7 +23,7 @@ __all__ = [
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_set_lr_ptr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_update", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -53,6 +53,7 @@ _SIGS = {
     "zero1_layout": (_I32, [_P, _P, _P, _P]),
     "zero1_bucket_begin": (_I32, [_P]),
     "zero1_bucket_reduce": (_I32, [_P, _U64, _U64, _P, _P]),
+    "zero1_bucket_update": (_I32, [_P, _U64, _U64, _P, _P, _P]),
     "zero1_bucket_finish": (_I32, [_P, _P, _P]),
     "zero1_profile_start": (_I32, [_P, _I32]),
     "zero1_profile_stop": (_I32, [_P, _P, _P, _P]),
@@ -279,8 +280,13 @@ def zero1_bucket_reduce(h: int, offset: int, count: int, grad_ptrs, stream=None)
     _check(_load().zero1_bucket_reduce(h, offset, count, _ptrs(grad_ptrs), _stream(stream)))
 
 
+def zero1_bucket_update(h: int, offset: int, count: int, grad_ptrs, param_ptrs, stream=None) -> None:
+    """Reduce-scatter and update one bucket (handles without clipping)."""
+    _check(_load().zero1_bucket_update(h, offset, count, _ptrs(grad_ptrs), _ptrs(param_ptrs), _stream(stream)))
+
+
 def zero1_bucket_finish(h: int, param_ptrs, stream=None) -> None:
-    _check(_load().zero1_bucket_finish(h, _ptrs(param_ptrs), _stream(stream)))
+    _check(_load().zero1_bucket_finish(h, None if param_ptrs is None else _ptrs(param_ptrs), _stream(stream)))
 
 
 def zero1_profile_start(h: int, capacity: int) -> None:

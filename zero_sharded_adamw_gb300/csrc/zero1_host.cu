@@ -78,6 +78,7 @@ struct zero1_ctx {
     // bucketed step (zero1_bucket_*): buckets in call order, their norm sums,
     // and a reduce-scatter scratch for W <= 2 (whose plain step re-reads)
     bool bucket_open = false;
+    int bucket_mode = 0;         // 0: no bucket yet, 1: reduce-only buckets, 2: reduce + update buckets
     std::vector<std::pair<uint64_t, uint64_t>> buckets;
     double *bucket_sums = nullptr;
     float *ghat_bucket = nullptr;
@@ -786,25 +787,44 @@ int zero1_bucket_begin(zero1_handle h)
         return cuda_fail(e, "cudaMalloc of the reduce-scatter scratch");
     }
     h->buckets.clear();
+    h->bucket_mode = 0;
     h->bucket_open = true;
     return ZERO1_OK;
 }
 
-int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, void *stream)
+namespace {
+
+// The checks every bucket of an open step passes: inside [0, n), an offset
+// on a vector boundary, a count that keeps the next bucket on one (only the
+// bucket that ends at n may be ragged), no overlap with an earlier bucket,
+// room in the table, and aligned per-rank pointers.
+int check_bucket(zero1_ctx *h, uint64_t offset, uint64_t count, const void *const *ptrs, int mode)
 {
-    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (!h->bucket_open) return fail(ZERO1_EINVAL, "no bucketed step is open (call zero1_bucket_begin)");
+    if (h->bucket_mode != 0 && h->bucket_mode != mode)
+        return fail(ZERO1_EINVAL, "one bucketed step uses zero1_bucket_reduce or zero1_bucket_update, not both");
     if (count == 0 || offset > h->n || count > h->n - offset)
         return fail(ZERO1_EINVAL, "bucket [%llu, +%llu) is outside [0, n)", (unsigned long long)offset,
                     (unsigned long long)count);
     if (offset % zero1::kVec) return fail(ZERO1_EINVAL, "bucket offsets must be multiples of 8");
+    if (count % zero1::kVec && offset + count != h->n)
+        return fail(ZERO1_EINVAL, "only the bucket that ends at n may have a count that is not a multiple of 8");
     if ((int)h->buckets.size() >= kMaxBuckets) return fail(ZERO1_EINVAL, "more than %d buckets", kMaxBuckets);
-    if (!grad_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (const auto &b : h->buckets)
+        if (offset < b.first + b.second && b.first < offset + count)
+            return fail(ZERO1_EINVAL, "bucket [%llu, +%llu) overlaps an earlier bucket", (unsigned long long)offset,
+                        (unsigned long long)count);
+    if (!ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
     for (int r = 0; r < h->world; ++r) {
-        if (!grad_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
-        if (!aligned16(grad_ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+        if (!ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
+        if (!aligned16(ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
     }
-    DeviceGuard g(h->device);
+    return ZERO1_OK;
+}
+
+// Reduce-scatter + norm partial of one bucket (K1 in bucket mode).
+int launch_bucket_rs(zero1_ctx *h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, cudaStream_t st)
+{
     zero1::StepLaunch s;
     s.grads = grad_ptrs;
     s.params = nullptr;
@@ -824,9 +844,66 @@ int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const v
     s.phase = 1;
     s.bucket_sums = h->bucket_sums;
     s.bucket_index = (int)h->buckets.size();
-    cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), nullptr);
+    cudaError_t e = zero1::launch_step(s, st, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return ZERO1_OK;
+}
+
+}  // namespace
+
+int zero1_bucket_reduce(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    int rc = check_bucket(h, offset, count, grad_ptrs, 1);
+    if (rc) return rc;
+    DeviceGuard g(h->device);
+    if ((rc = launch_bucket_rs(h, offset, count, grad_ptrs, static_cast<cudaStream_t>(stream)))) return rc;
+    h->buckets.emplace_back(offset, count);
+    h->bucket_mode = 1;
+    return ZERO1_OK;
+}
+
+int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const void *const *grad_ptrs,
+                        void *const *param_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    if (h->hp.max_norm > 0.0)
+        return fail(ZERO1_EINVAL, "zero1_bucket_update needs clipping off (max_norm <= 0): a clipped update "
+                                  "waits for the global norm (use zero1_bucket_reduce)");
+    if (h->bctab) return fail(ZERO1_EINVAL, "zero1_bucket_update is not available on a capturable handle");
+    int rc = check_bucket(h, offset, count, grad_ptrs, 2);
+    if (rc) return rc;
+    if ((rc = check_bucket(h, offset, count, param_ptrs, 2))) return rc;
+    DeviceGuard g(h->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = launch_bucket_rs(h, offset, count, grad_ptrs, st))) return rc;
+    // The update of the bucket's parameters right away (c = 1 without
+    // clipping); CTA 0 also records the norm of the buckets so far.
+    zero1::StepLaunch s;
+    s.grads = nullptr;
+    s.params = param_ptrs;
+    s.world = h->world;
+    s.n = count;
+    s.master = h->master + offset;
+    s.m = h->m + offset * h->msz;
+    s.v = h->v + offset * h->msz;
+    s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    if (h->opts.bucket_ctas > 0 && s.grid_update > h->opts.bucket_ctas) s.grid_update = h->opts.bucket_ctas;
+    s.moments_bf16 = h->opts.moments_bf16 != 0;
+    s.decay_first = h->opts.decay_before_update != 0;
+    s.clip_eps = h->opts.clip_eps;
+    s.phase = 2;
+    s.bucket_sums = h->bucket_sums;
+    s.nbuckets = (int)h->buckets.size() + 1;
+    cudaError_t e = zero1::launch_step(s, st, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     h->buckets.emplace_back(offset, count);
+    h->bucket_mode = 2;
     return ZERO1_OK;
 }
 
@@ -834,10 +911,13 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (!h->bucket_open) return fail(ZERO1_EINVAL, "no bucketed step is open");
-    if (!param_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
-    for (int r = 0; r < h->world; ++r) {
-        if (!param_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
-        if (!aligned16(param_ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+    const bool updated = h->bucket_mode == 2;   // every bucket already updated its parameters
+    if (!updated) {
+        if (!param_ptrs) return fail(ZERO1_EINVAL, "pointer array is NULL");
+        for (int r = 0; r < h->world; ++r) {
+            if (!param_ptrs[r]) return fail(ZERO1_EINVAL, "rank %d buffer is NULL", r);
+            if (!aligned16(param_ptrs[r])) return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
+        }
     }
     std::vector<std::pair<uint64_t, uint64_t>> sorted = h->buckets;
     std::sort(sorted.begin(), sorted.end());
@@ -849,6 +929,11 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
     if (next != h->n) {
         h->bucket_open = false;
         return fail(ZERO1_EINVAL, "the buckets must cover [0, n) exactly once; the bucketed step is abandoned");
+    }
+    if (updated) {
+        h->bucket_open = false;
+        h->t += 1;
+        return ZERO1_OK;
     }
     DeviceGuard g(h->device);
     zero1::StepLaunch s;

@@ -652,6 +652,10 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     // shared-memory accesses are consecutive (no bank conflicts).
     const float c = sm.clip;
     const StepScalars sc = sm.sc;
+    // Discards act on whole 128-byte L2 lines, so only when ĝ starts on a
+    // line: a bucket that begins mid-line (a multiple of 8 parameters, not
+    // of 32) must not drop its neighbour's unread values.
+    const bool discard = !REREAD && (reinterpret_cast<uintptr_t>(p.ghat) & 127u) == 0;
     uint32_t k = 0;
     for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
         const int s = k % kUpdStages;
@@ -659,7 +663,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint64_t base = (uint64_t)j * kUpdTile;
         const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kUpdTile ? nel - base : kUpdTile);
-        if (!REREAD && threadIdx.x < cnt / 32u) {
+        if (discard && threadIdx.x < cnt / 32u) {
             // This tile's ĝ is in shared memory now and dead in HBM: drop its
             // whole 128-byte lines from L2 unwritten (a partly covered last
             // line may hold the n % 8 tail and is left alone).
