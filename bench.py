@@ -587,6 +587,70 @@ def zero2_arm(args, w: WL.Workload):
     print(json.dumps(line), flush=True)
 
 
+def ddp_arm(args, w: WL.Workload):
+    """The DDP baseline the ZeRO-1 step is measured against: the bf16
+    gradients all-reduced (mean, in place, zero1_allreduce), then every rank
+    runs the full AdamW on its own replicated optimizer state (W handles of
+    world 1, zero1_step).  Emulated on one GPU the W ranks' work is summed,
+    so the figure compares total GPU work and optimizer-state memory:
+    DDP holds W copies of master/m/v, ZeRO-1 one sharded copy."""
+    import zero_sharded_adamw_gb300 as z
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    hp = z.Hparams(**w.hparams())
+    grads = WL.grads(w, 1, dev)
+    reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
+    m0 = WL.master(w, dev)
+    ranks = [z.Zero1(w.n, 1, hp, z.Options(small_step=-1)) for _ in range(w.world)]
+    for h in ranks:
+        h.set_state(m0, stream=stream)
+    zero1 = z.Zero1(w.n, w.world, hp)
+    zero1.set_state(m0, stream=stream)
+    rep_tables = [z.PtrTable([r]) for r in reps]
+    grad_tables = [z.PtrTable([g]) for g in grads]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def ddp_step():
+        z.zero1_allreduce(w.n, w.world, z.DTYPE_BF16, z.OP_AVG, grads, grads, err, stream)
+        for q, h in enumerate(ranks):
+            h.step(grad_tables[q], rep_tables[q], stream)
+
+    def zero1_step():
+        zero1.step(grads, reps, stream)
+
+    out = {}
+    for name, fn in (("ddp", ddp_step), ("zero1", zero1_step)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = e0.elapsed_time(e1) / args.steps
+    assert int(err.item()) == 0, "a kernel pipeline wait gave up"
+    state_ddp = sum(h.layout()[2] for h in ranks)
+    state_zero1 = zero1.layout()[2]
+    for h in ranks + [zero1]:
+        h.close()
+    line = {
+        "metric": "DDP baseline vs ZeRO-1: step ms (all W emulated ranks' work) and optimizer-state bytes",
+        "value": out["ddp"], "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
+                   "ddp": "bf16 all-reduce (mean, in place) + W replicated AdamW updates",
+                   "note": "the gradients are overwritten by their mean each step (timing only)"},
+        "ms": {"ddp_step": out["ddp"], "zero1_step": out["zero1"]},
+        "optimizer_state_bytes": {"ddp_all_ranks": state_ddp, "zero1_all_ranks": state_zero1},
+        "gpu_launches": args.steps * (1 + 2 * w.world),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def fsdp_arm(args):
     """ZeRO-3 / FSDP forward over the GPT-2-small layers (embeddings + 12
     blocks), W = 8 emulated ranks: each layer's bf16 parameters are sharded
@@ -700,7 +764,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="step", choices=["step", "allreduce", "zero2", "fsdp"],
+    ap.add_argument("--path", default="step", choices=["step", "allreduce", "zero2", "fsdp", "ddp"],
                     help="step: the ZeRO-1 optimizer step (default); allreduce: the DDP all-reduce; "
                          "zero2: the bucketed step overlapped with an emulated backward; "
                          "fsdp: per-layer parameter all-gather with prefetch")
@@ -745,6 +809,8 @@ def main(argv=None):
         zero2_arm(args, w)
     elif args.path == "fsdp" and args.impl == "ours":
         fsdp_arm(args)
+    elif args.path == "ddp" and args.impl == "ours":
+        ddp_arm(args, w)
     elif args.impl == "reference":
         reference_arm(args, w, cfg)
     else:
