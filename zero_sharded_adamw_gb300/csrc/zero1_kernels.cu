@@ -712,14 +712,15 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 // Small steps: the whole step in one launch of one thread-block cluster.
 // Each thread owns up to VPT 8-parameter vectors (vector i of thread g of
 // the cluster is g + i * kSmallCtas * kSmallThreads, threads numbered with
-// the warps interleaved over the CTAs).  It loads their
-// master, m, v and their W gradients (in batches of loads issued before
-// any add), forms the rank-ordered mean and its squares, and keeps both in
-// registers; the CTAs' fixed-order partial sums meet through distributed
-// shared memory, every CTA adds the kSmallCtas partials in rank order (so
-// all form the same c), and each thread then updates its vectors and
-// stores master, m, v and the W replicas.  The cluster barrier is a hardware barrier that every thread
-// reaches: nothing returns early.
+// the warps interleaved over the CTAs).  It loads their master, m, v and
+// their W gradients (in batches of loads issued before any add), forms the
+// rank-ordered mean and its squares, and keeps both in registers.  Each
+// CTA pushes its fixed-order partial sums into every CTA's shared memory
+// (distributed shared memory), one cluster barrier makes them visible,
+// every CTA adds the kSmallCtas partials in rank order (so all form the
+// same c), and each thread then updates its vectors and stores master, m,
+// v and the W replicas.  The cluster barriers are hardware barriers that
+// every thread reaches: nothing returns early.
 template <int CAP>
 struct SmallParams {
     const uint16_t *grads[CAP];
@@ -768,7 +769,7 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
     constexpr int kWarps = THREADS / 32;
     constexpr uint32_t kStride = CTAS * THREADS;
     __shared__ double red_a[kWarps], red_b[kWarps];
-    __shared__ double part[2];
+    __shared__ double part[2 * CTAS];      // (sum, plain sum) of every CTA, in cluster rank order
     __shared__ float clip;
     __shared__ StepScalars ssc;
     const int nw = W > 0 ? W : p.world;
@@ -778,8 +779,12 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
     // every SM of the cluster; each warp still covers 32 consecutive vectors.
     const uint32_t gt = ((threadIdx.x >> 5) * CTAS + blockIdx.x) * 32u + (threadIdx.x & 31u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Every CTA of the cluster must have started before any thread writes
+    // into another CTA's shared memory: arrive now, wait just before the
+    // pushes below (by then the wait is free).
+    cluster_arrive_relaxed();
     // Capturable: this step is t + 1; every CTA reads t here, before the
-    // first cluster barrier, and CTA 0 advances it after the second.
+    // cluster barrier, and CTA 0 advances it after it.
     const unsigned long long tnext = p.dev.bc ? p.status->t + 1 : 0ull;
     if (threadIdx.x == 0) ssc = p.dev.bc ? form_scalars(p.sc, p.dev, tnext) : p.sc;
 
@@ -857,38 +862,36 @@ zero1_small_step_kernel(const __grid_constant__ SmallParams<CAP> p)
         red_b[warp] = b;
     }
     __syncthreads();
+    cluster_wait();            // every CTA has started (the arrive at the top)
     if (threadIdx.x == 0) {
         double x = 0.0, y = 0.0;
         for (int i = 0; i < kWarps; ++i) {
             x += red_a[i];
             y += red_b[i];
         }
-        part[0] = x;
-        part[1] = y;
-    }
-    static_assert(CTAS > 1 && CTAS <= 32, "a cluster of 2..32 CTAs (one lane per CTA below)");
-    cluster_sync();            // every CTA's partials are written
-    if (warp == 0) {
-        // Lane r fetches CTA r's pair (one remote round trip for all), then
-        // lane 0 adds them in rank order.
-        double pa = 0.0, pb = 0.0;
-        if (lane < CTAS) {
-            pa = ld_cluster_f64(&part[0], (uint32_t)lane);
-            pb = ld_cluster_f64(&part[1], (uint32_t)lane);
+        // Push this CTA's pair into slot blockIdx.x (its cluster rank) of
+        // every CTA's table, this CTA's own included.
+        for (uint32_t r = 0; r < (uint32_t)CTAS; ++r) {
+            st_cluster_f64(&part[2 * blockIdx.x], r, x);
+            st_cluster_f64(&part[2 * blockIdx.x + 1], r, y);
         }
+    }
+    static_assert(CTAS > 1 && CTAS <= 32, "a cluster of 2..32 CTAs");
+    // The pushes (released before this barrier) are visible after it, and
+    // no CTA touches another's shared memory afterwards, so a CTA may finish
+    // while the others still work.
+    cluster_sync();
+    if (threadIdx.x == 0) {
         double x = 0.0, y = 0.0;
-#pragma unroll
-        for (int r = 0; r < CTAS; ++r) {
-            x += __shfl_sync(0xFFFFFFFFu, pa, r);
-            y += __shfl_sync(0xFFFFFFFFu, pb, r);
+        for (int r = 0; r < CTAS; ++r) {       // rank order: every CTA forms the same c
+            x += part[2 * r];
+            y += part[2 * r + 1];
         }
-        if (lane == 0) {
-            float c;
-            finish_norm(x, y, p.max_norm, p.clip_eps, blockIdx.x == 0 ? p.status : nullptr, &c);
-            clip = c;
-        }
+        float c;
+        finish_norm(x, y, p.max_norm, p.clip_eps, blockIdx.x == 0 ? p.status : nullptr, &c);
+        clip = c;
     }
-    cluster_sync();            // all remote reads are done (no CTA leaves early); `clip` is visible
+    __syncthreads();
     const float c = clip;
     const StepScalars sc = ssc;
     const bool decay_first = p.decay_first != 0;

@@ -186,6 +186,15 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, for work between them: arrive
+// (relaxed: no memory ordering), and later wait for every thread of every
+// CTA of the cluster to have arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
+
 // The double at the same shared-memory offset as `local`, in the CTA of
 // cluster rank `rank` (distributed shared memory).
 __device__ __forceinline__ double ld_cluster_f64(const double *local, uint32_t rank)
@@ -195,6 +204,15 @@ __device__ __forceinline__ double ld_cluster_f64(const double *local, uint32_t r
     double v;
     asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
     return v;
+}
+
+// Store a double at the same shared-memory offset as `local`, in the CTA of
+// cluster rank `rank` (distributed shared memory).
+__device__ __forceinline__ void st_cluster_f64(double *local, uint32_t rank, double v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(remote), "d"(v) : "memory");
 }
 
 // ------------------------------------------------------------ bf16 pack
