@@ -12,7 +12,6 @@ import subprocess
 import numpy as np
 import pytest
 
-import zero_sharded_adamw_gb300 as z
 from oracle import zero1_oracle as o
 from zero_sharded_adamw_gb300 import _build
 
