@@ -42,11 +42,12 @@
  * Parity pins: every function below is pinned by the not-gpu tests against
  * the pages' printed values, closed forms, torch.optim.AdamW special cases,
  * numpy/torch library routines and brute force (see tests/test_oracle_*.py).
- * One exception, "parity unpinned": the intermediate bf16 roundings of the
- * bf16-moment variant (zref_adamw_range_ex with moments_bf16).  The pages
- * only say that some configurations store m and v in bf16; the per-op
- * rounding sequence is a reading, tied to the fp32-moment oracle by bounds
- * and to closed forms only within bf16 precision.
+ * The bf16-moment variant (zref_adamw_range_ex with moments_bf16) is a
+ * reading: the pages only say that some configurations store m and v in
+ * bf16.  Its m and v rounding sequence is pinned to the page's in-place
+ * ops run by torch on bf16 tensors.  One part remains "parity unpinned":
+ * the rounding of the denominator d = bf16(bf16(sqrt(v)) + eps), which is
+ * tied to the fp32-moment oracle by bounds and closed forms only.
  */
 #include <stdint.h>
 #include <string.h>

@@ -49,6 +49,10 @@ MUTANTS = {
     "variant_decay_order_ignored": ("        if (o->decay_before_update) {", "        if (0) {"),
     "variant_clip_eps_ignored": ("    double q = max_norm / (norm + clip_eps);", "    double q = max_norm / norm;"),
     "variant_bf16_v_not_stored": ("            vb[i] = zref_f32_to_bf16(vi);", "            (void)vb;"),
+    "variant_bf16_m_product_not_rounded": ("mi = bf16_round(s->beta1 * zref_bf16_to_f32(mb[i]));",
+                                           "mi = s->beta1 * zref_bf16_to_f32(mb[i]);"),
+    "variant_bf16_v_product_not_rounded": ("vi = bf16_round(s->beta2 * zref_bf16_to_f32(vb[i]));",
+                                           "vi = s->beta2 * zref_bf16_to_f32(vb[i]);"),
     "gather_shards_off_by_one": ("uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len;",
                                  "uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len - 1;"),
     "stage1_not_sharded": ("case 1: return (2.0 + 2.0) * psi + k * psi / w;", "case 1: return (2.0 + 2.0 + k) * psi;"),
