@@ -107,7 +107,9 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     configurations keep them in bf16: 12 bytes per parameter in all); each
  *     moment update computes in fp32 and rounds to bf16 per operation:
  *     m = bf16(bf16(b1*m) + (1-b1)*g), v = bf16(bf16(b2*v) + (1-b2)*g*g),
- *     d = bf16(bf16(sqrt(v)) + eps); the fp32 master update uses those.
+ *     d = bf16(bf16(sqrt(v)) + bf16(eps)) (a scalar added to a bf16 tensor
+ *     is rounded to bf16, as torch does); the fp32 master update uses
+ *     those.
  *   bucket_ctas: CTAs of each zero1_bucket_reduce launch (0 = one per SM).
  *     Fewer leave SMs to a backward running alongside on another stream.
  *   small_step: the one-launch path for small n (a single thread-block

@@ -44,10 +44,11 @@
  * numpy/torch library routines and brute force (see tests/test_oracle_*.py).
  * The bf16-moment variant (zref_adamw_range_ex with moments_bf16) is a
  * reading: the pages only say that some configurations store m and v in
- * bf16.  Its m and v rounding sequence is pinned to the page's in-place
- * ops run by torch on bf16 tensors.  One part remains "parity unpinned":
- * the rounding of the denominator d = bf16(bf16(sqrt(v)) + eps), which is
- * tied to the fp32-moment oracle by bounds and closed forms only.
+ * bf16.  It is the page's in-place ops applied to bf16 tensors, as torch
+ * performs them: each op computes in fp32 and rounds its result to bf16,
+ * and a scalar added to a bf16 tensor (eps) is rounded to bf16 first.
+ * The tests pin that sequence, m, v, the denominator and the master, to
+ * torch running those ops.
  */
 #include <stdint.h>
 #include <string.h>
@@ -300,7 +301,8 @@ void zref_adamw_range_ex(float *master, void *m, void *v, const float *ghat, uin
             vi = bf16_round(s->beta2 * zref_bf16_to_f32(vb[i]));
             float og = s->one_minus_beta2 * g;
             vi = bf16_round(vi + og * g);
-            d = bf16_round(bf16_round(sqrtf(vi)) + s->eps);
+            /* eps joins a bf16 tensor: torch rounds the scalar to bf16 */
+            d = bf16_round(bf16_round(sqrtf(vi)) + bf16_round(s->eps));
             mb[i] = zref_f32_to_bf16(mi);
             vb[i] = zref_f32_to_bf16(vi);
         } else {

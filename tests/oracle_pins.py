@@ -534,29 +534,39 @@ def pin_bf16_moments_bounds():
 
 def pin_bf16_moments_vs_torch_inplace_ops():
     """The bf16-moment reading against the page's own in-place ops run by
-    torch on bf16 tensors: m.mul_(b1).add_(g, alpha=1-b1) and
-    v.mul_(b2).addcmul_(g, g, value=1-b2), each op computing in fp32 and
-    rounding its result to bf16.  Step by step from the oracle's state, the
-    oracle's m and v equal torch's in at least 99.9% of the elements.
-    Torch's kernels fuse the multiply-add before that rounding, where the
-    reading rounds the product to fp32 first.  That moves a value lying at
-    a bf16 rounding boundary by one bf16 ulp, or leaves a residual of the
-    product's fp32 rounding where the two terms cancel exactly.  Every
-    difference is within those bounds.  A reading without the intermediate
-    rounding disagrees in most elements."""
+    torch on bf16 tensors: m.mul_(b1).add_(g, alpha=1-b1),
+    v.mul_(b2).addcmul_(g, g, value=1-b2) and denom = v.sqrt().add_(eps),
+    each op computing in fp32 and rounding its result to bf16; the fp32
+    master then takes p - step_size * (m / denom) and the decay, one fp32
+    operation at a time.  Step by step from the oracle's state, the oracle's
+    m, v and master equal torch's in at least 99.9% of the elements
+    (eps = 1e-3, near sqrt(v), so that the roundings of d matter).
+    Torch's kernels fuse the moments' multiply-add before the bf16
+    rounding, where the reading rounds the product to fp32 first.  That
+    moves a value lying at a bf16 rounding boundary by one bf16 ulp, or
+    leaves a residual of the product's fp32 rounding where the two terms
+    cancel exactly.  Every moment difference is within those bounds.  A
+    reading without an intermediate rounding disagrees in most elements."""
     rng = np.random.default_rng(41)
     n = 20_000
     opts = o.Options(moments_bf16=True)
-    hp = o.HP(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.0)
+    hp = o.HP(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-3, weight_decay=0.1, max_norm=0.0)
     st = o.state_ex((rng.standard_normal(n) * 0.02).astype(np.float32), opts)
     as_bf16 = lambda u: torch.from_numpy(u.astype(np.uint16).view(np.int16).copy()).view(torch.bfloat16)
     bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
-    for _ in range(6):
+    for t in range(1, 7):
         g = rand_bf16(rng, n, 1e-2)
         gt = torch.from_numpy(torch_widen(g).astype(np.float32))
         m, v = as_bf16(st.m), as_bf16(st.v)
+        p = torch.from_numpy(st.master.copy())
+        sc = o.step_scalars(hp, 1, t)
         m.mul_(hp.beta1).add_(gt, alpha=1 - hp.beta1)
         v.mul_(hp.beta2).addcmul_(gt, gt, value=1 - hp.beta2)
+        denom = v.sqrt().add_(hp.eps)
+        u = m.float() / denom.float()
+        p = p - torch.tensor(sc["step_size"], dtype=torch.float32) * u
+        p = p * torch.tensor(sc["decay"], dtype=torch.float32)
+        assert st.t == t - 1
         o.step_ex(st, [g], hp, opts)                       # W = 1, no clipping: the step sees g exactly
         gw = torch_widen(g).astype(np.float64)
         for ours, theirs, term in ((st.m, bits(m), (1 - hp.beta1) * np.abs(gw)),
@@ -565,6 +575,7 @@ def pin_bf16_moments_vs_torch_inplace_ops():
             a64, b64 = torch_widen(ours).astype(np.float64), torch_widen(theirs).astype(np.float64)
             tol = 2.0 ** -7 * np.maximum(np.abs(a64), np.abs(b64)) + 2.0 ** -23 * term
             assert (np.abs(a64 - b64) <= tol).all()
+        assert np.mean(st.master.view(np.uint32) == p.numpy().view(np.uint32)) >= 0.999
 
 
 def pin_ddp_linearity():

@@ -53,6 +53,10 @@ MUTANTS = {
                                            "mi = s->beta1 * zref_bf16_to_f32(mb[i]);"),
     "variant_bf16_v_product_not_rounded": ("vi = bf16_round(s->beta2 * zref_bf16_to_f32(vb[i]));",
                                            "vi = s->beta2 * zref_bf16_to_f32(vb[i]);"),
+    "variant_bf16_sqrt_not_rounded": ("d = bf16_round(bf16_round(sqrtf(vi)) + bf16_round(s->eps));",
+                                      "d = bf16_round(sqrtf(vi) + bf16_round(s->eps));"),
+    "variant_bf16_eps_not_rounded": ("d = bf16_round(bf16_round(sqrtf(vi)) + bf16_round(s->eps));",
+                                     "d = bf16_round(bf16_round(sqrtf(vi)) + s->eps);"),
     "gather_shards_off_by_one": ("uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len;",
                                  "uint64_t lo = (uint64_t)r * shard_len, hi = lo + shard_len - 1;"),
     "stage1_not_sharded": ("case 1: return (2.0 + 2.0) * psi + k * psi / w;", "case 1: return (2.0 + 2.0 + k) * psi;"),

@@ -148,6 +148,29 @@ zero1::StepScalars step_scalars(const zero1_hparams &hp, int world, uint64_t t)
     return s;
 }
 
+// Round-to-nearest-even float -> bf16 -> float (finite values).
+float round_to_bf16(float x)
+{
+    uint32_t u;
+    std::memcpy(&u, &x, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    u &= 0xFFFF0000u;
+    float r;
+    std::memcpy(&r, &u, sizeof r);
+    return r;
+}
+
+// The scalars one launch of this handle uses for step t.  With bf16
+// moments, d = sqrt(v) + eps is an in-place add of the scalar eps to a bf16
+// tensor, which torch performs with eps rounded to bf16; the step does
+// the same.
+zero1::StepScalars launch_scalars(const zero1_ctx *h, uint64_t t)
+{
+    zero1::StepScalars s = step_scalars(h->hp, h->world, t);
+    if (h->opts.moments_bf16) s.eps = round_to_bf16(s.eps);
+    return s;
+}
+
 constexpr uint64_t kMaxBiasTable = 1ull << 22;   // entries (64 MiB) a capturable handle may tabulate
 
 // The step's scalars as a capturable launch forms them on the device.
@@ -395,7 +418,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.ghat = h->ghat;
     s.partials = h->partials;
     s.status = h->status;
-    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
     s.grid_rs = h->grid_rs;
     s.grid_update = h->grid_update;
@@ -836,7 +859,7 @@ int launch_bucket_rs(zero1_ctx *h, uint64_t offset, uint64_t count, const void *
     s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
     s.partials = h->partials;
     s.status = h->status;
-    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
     s.clip_eps = h->opts.clip_eps;
     zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
@@ -890,7 +913,7 @@ int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const v
     s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
     s.partials = h->partials;
     s.status = h->status;
-    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
     zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
     if (h->opts.bucket_ctas > 0 && s.grid_update > h->opts.bucket_ctas) s.grid_update = h->opts.bucket_ctas;
@@ -947,7 +970,7 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
     s.ghat = h->ghat ? h->ghat : h->ghat_bucket;
     s.partials = h->partials;
     s.status = h->status;
-    s.sc = step_scalars(h->hp, h->world, h->t + 1);
+    s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
     s.grid_rs = h->grid_rs;
     s.grid_update = h->grid_update;
