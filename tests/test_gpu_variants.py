@@ -142,3 +142,41 @@ def test_bf16_moments_footprint_and_checkpoint():
         resumed = _moments(c, n, True)
     for x, y in zip(full, resumed):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_bf16_moments_range_checkpoint():
+    """Per-shard save and load of bf16 moments (the range forms address m and
+    v in 2-byte elements) resumes bit for bit."""
+    n, world = 50_003, 4
+    w = WL.Workload("ckr", n, world, 0.01, 6, max_norm=0.05)
+    zo = z.Options(moments_bf16=True, small_step=-1)
+    hp = z.Hparams(**w.hparams())
+    m0 = WL.master(w, "cuda")
+    grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    reps = [torch.empty_like(grads[0]) for _ in range(world)]
+    with z.Zero1(n, world, hp, zo) as a:
+        a.set_state(m0)
+        for t in range(1, 7):
+            a.step(WL.grads(w, t, "cuda", out=grads), reps)
+        full = _moments(a, n, True)
+    with z.Zero1(n, world, hp, zo) as b:
+        b.set_state(m0)
+        for t in range(1, 4):
+            b.step(WL.grads(w, t, "cuda", out=grads), reps)
+        s, _, _ = b.layout()
+        saved = [np.zeros(n, np.float32), np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
+        for r in range(world):
+            lo, hi = min(r * s, n), min((r + 1) * s, n)
+            z.zero1_get_state_range(b.handle, lo, hi - lo, *[x[lo:] for x in saved])
+        torch.cuda.synchronize()
+        tsave = b.get_state()
+    with z.Zero1(n, world, hp, zo) as c:
+        c.set_state(np.zeros(n, np.float32), t=tsave)     # t only; every element is then loaded per shard
+        for r in range(world):
+            lo, hi = min(r * s, n), min((r + 1) * s, n)
+            z.zero1_set_state_range(c.handle, lo, hi - lo, *[x[lo:] for x in saved])
+        for t in range(4, 7):
+            c.step(WL.grads(w, t, "cuda", out=grads), reps)
+        resumed = _moments(c, n, True)
+    for x, y in zip(full, resumed):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
