@@ -82,7 +82,10 @@ typedef struct zero1_hparams {
 
 typedef struct zero1_ctx *zero1_handle;
 
-/* Create an optimizer for n parameters over `world` emulated ranks.
+/* Create an optimizer for n parameters over `world` emulated ranks
+ * ("Stanford CS336 Lecture 7 close reading: Parallelism (part 1)", section
+ * 5.2: under ZeRO stage 1 each rank keeps the optimizer state of its own
+ * slice of the parameters only).
  * Allocates the fp32 master, m and v (each W*S floats, S the shard length
  * below) plus scratch on the current CUDA device with cudaMalloc; m = v = 0,
  * master = 0, t = 0.  Load real weights with zero1_set_state.
@@ -160,7 +163,11 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
  * NULL is accepted and ignored.  Returns ZERO1_OK or ZERO1_ECUDA. */
 int zero1_destroy(zero1_handle h);
 
-/* One ZeRO-1 step (t -> t+1) on `stream`, fully asynchronous, allocation-free.
+/* One ZeRO-1 step (t -> t+1) on `stream`, fully asynchronous, allocation-free
+ * ("Stanford CS336 Lecture 7 close reading: Parallelism (part 1)", section
+ * 5.2: reduce-scatter the gradients, update each rank's slice with its own
+ * optimizer state, all-gather the updated parameters; the update itself as
+ * "Parallel training", "What one card holds: mixed precision and AdamW").
  *   grad_ptrs:  host array of W device pointers; rank r's bf16 gradient,
  *               n entries, 16-byte aligned.  Only read.
  *   param_ptrs: host array of W device pointers; rank r's bf16 parameter
@@ -260,7 +267,9 @@ int zero1_host_sync(zero1_handle h);
 int zero1_set_state(zero1_handle h, const float *master, const void *m, const void *v,
                     uint64_t t, void *stream);
 
-/* Checkpoint save: copies master, m, v (n fp32 each) into device or host
+/* Checkpoint save ("Parallel training", "Training loop and checkpoint": a
+ * checkpoint must hold m, v and the step count t, or bias correction
+ * restarts from t = 1 without the moments): copies master, m, v (n fp32 each) into device or host
  * arrays (any may be NULL to skip it) and writes the step count to *t (may
  * be NULL).  Enqueued on `stream`; synchronize it before reading a host
  * destination.  On a capturable handle t is read from the device counter
@@ -294,7 +303,14 @@ int zero1_set_lr(zero1_handle h, double lr);
 int zero1_set_lr_ptr(zero1_handle h, const double *device_lr);
 
 /* Norm of the averaged gradient of the latest step and the clip coefficient
- * it applied (1 when not clipped).  Waits for `stream`.  Either output may
+ * it applied (1 when not clipped) ("Parallel training", "Training loop and
+ * checkpoint": the gradient is clipped by its global L2 norm, scaled down
+ * when the norm exceeds max_norm).  The norm is returned in double because
+ * the kernels finish it in fp64; the coefficient is the fp32 value the
+ * update multiplied into every gradient element, so a caller (or a test)
+ * can repeat the update exactly.  Both live in device memory written by the
+ * step's kernels, so the read is ordered on `stream`, the stream the step
+ * ran on, and waits for it.  Either output may
  * be NULL.  Before the first step both read 0.  Returns ZERO1_ECUDA if any
  * step of this handle had a kernel pipeline wait give up (each wait is
  * bounded to 1 s so that a fault cannot hang the GPU); the state is then not
@@ -359,10 +375,15 @@ int zero1_step_scalars(const zero1_hparams *hp, int world, uint64_t t, float out
  * fixed ~16.1 MiB array inside the library image, held by every GPU that
  * loads the library until the process exits.  The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress) with the
- * device current; make that first call before any stream capture.  Each
- * call clears the scratch status on `stream` first.  All calls share the
- * one array: calls whose GPU work overlaps (other streams or threads) race.
- * The norm is not read back by this call.
+ * device current; make that first call before any stream capture.  The
+ * address is kept with the identity of the CUDA context it belongs to, and
+ * a call made in another context (for instance after cudaDeviceReset)
+ * looks it up again.  Each call clears the scratch status on `stream`
+ * first.  All calls share the one array: calls whose GPU work overlaps
+ * (other streams or threads) race.  The norm is not read back by this
+ * call, and neither is the bit a kernel pipeline wait sets when it gives up
+ * after its 1 s limit: a timeout on this path is not reported (the next
+ * call clears it).
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ENODEV, ZERO1_ECUDA. */
 int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp, uint64_t t,
                        const void *const *grad_ptrs, void *const *param_ptrs,

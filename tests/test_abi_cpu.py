@@ -195,3 +195,44 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
         with pytest.raises(z.Zero1Error) as e:
             call()
         assert e.value.code == -5 and "not built" in str(e.value)
+
+
+def test_binding_checks_pointer_counts_and_buffers(lib_path):
+    """The binding refuses, before any C call, a pointer list whose length
+    differs from the world size the C side reads, and buffers of the wrong
+    type, place or size (the C side would read past the host array or hand
+    the kernels addresses they cannot use)."""
+    bf = lambda k: torch.zeros(k, dtype=torch.bfloat16)          # host tensors: never reach a kernel
+    f32 = lambda k: torch.zeros(k, dtype=torch.float32)
+    hp = z.Hparams()
+    with pytest.raises(ValueError, match="3 pointers given, the call reads 4"):
+        z.zero1_allreduce(16, 4, z.DTYPE_BF16, z.OP_SUM, [bf(16)] * 3, [bf(16)] * 4)
+    with pytest.raises(ValueError, match="pointers given"):
+        z.zero1_allgather(16, 4, 8, z.DTYPE_BF16, [0] * 4, [bf(16)] * 5)
+    with pytest.raises(ValueError, match="pointers given"):
+        z.zero1_step_noalloc(16, 2, hp, 1, [bf(16)], [bf(16)] * 2, f32(16), f32(16), f32(16))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        z.zero1_allreduce(16, 2, z.DTYPE_BF16, z.OP_SUM, [bf(16)] * 2, [bf(16)] * 2)
+    with pytest.raises(ValueError, match="expected torch.float32"):
+        z.zero1_step_noalloc(16, 2, hp, 1, [0, 0], [0, 0], bf(16), f32(16), f32(16))
+    with pytest.raises(ValueError, match="elements, the call reads or writes 16"):
+        z._check_buffer(f32(15), 16, "f32", None, "master")
+    # host-buffer entry points want host memory of n entries per rank
+    z._HANDLES[12345] = (16, 2, False)
+    try:
+        with pytest.raises(ValueError, match="pointers given"):
+            z.zero1_step_host(12345, [bf(16)], [bf(16)] * 2)
+        with pytest.raises(ValueError, match="elements, the call reads or writes 16"):
+            z.zero1_step_host(12345, [bf(16), bf(8)], [bf(16)] * 2)
+        with pytest.raises(ValueError, match="expected torch.float32"):
+            z.zero1_get_state(12345, bf(16))
+        with pytest.raises(ValueError, match="pointers given"):
+            z.zero1_step(12345, z.PtrTable([0]), z.PtrTable([0, 0]))
+    finally:
+        z._HANDLES.pop(12345)
+    # numpy host arrays are checked by element size and count
+    with pytest.raises(ValueError, match="4-byte elements"):
+        z._check_buffer(np.zeros(16, np.float32), 16, "bf16", False, "x")
+    with pytest.raises(ValueError, match="host memory"):
+        z._check_buffer(np.zeros(16, np.uint16), 16, "bf16", True, "x")
+    z._check_buffer(np.zeros(16, np.uint16), 16, "bf16", False, "x")

@@ -8,7 +8,9 @@ library.  This test calls it through the C ABI twice in a row (steps 1 and
 2) and checks each result against the handle-based zero1_step run on the
 same inputs, within the tolerance the parity tests use (1e-6 relative on the
 fp32 state, 1 bf16 ulp on the replicas); with the same kernels and grid the
-two should in fact agree bit for bit, which is checked as well.  It must pass
+two should in fact agree bit for bit, which is checked as well.  Each call
+is also checked directly against the CPU oracle running the same steps with
+its own norm and clip coefficient, within the same tolerance.  It must pass
 alone in a fresh process and after every other test, so it depends on no
 state another test leaves behind.  The file sorts last so that a run that
 stops at the first failure has run everything else first.
@@ -21,6 +23,7 @@ import torch
 
 import workloads as WL
 import zero_sharded_adamw_gb300 as z
+from oracle import zero1_oracle as o
 from tests.gpu_util import bf16_ulp, bits_equal, f32, rel_err, u16
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +56,7 @@ def test_noalloc_matches_handle_step_on_two_calls(n, world):
     m = torch.zeros_like(master)
     v = torch.zeros_like(master)
     reps_b = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    oracle = o.State(f32(m0))
     for t in (1, 2):
         z.zero1_step_noalloc(n, world, hp, t, grads[t], reps_b, master, m, v)
         torch.cuda.synchronize()
@@ -64,12 +68,20 @@ def test_noalloc_matches_handle_step_on_two_calls(n, world):
         for ra, rb in zip(got[3], want[3]):
             assert bf16_ulp(ra, rb) <= 1
             assert np.array_equal(ra, rb)
+        # the oracle, free-running on the same gradients
+        reps_o, _, _ = o.step(oracle, [u16(g) for g in grads[t]], o.HP(**w.hparams()))
+        for a, b in zip(got[:3], (oracle.master, oracle.m, oracle.v)):
+            assert rel_err(a, b) <= TOL
+        for ra, rb in zip(got[3], reps_o):
+            assert bf16_ulp(ra, rb) <= 1
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     n, world = (1 << 22) + 1, 2
-    g = [torch.zeros(8, dtype=torch.bfloat16, device="cuda")] * world
-    s = torch.zeros(8, device="cuda")
+    # raw addresses: the binding cannot size-check them, so the C entry
+    # point's own limit check is what answers
+    g = [torch.zeros(8, dtype=torch.bfloat16, device="cuda").data_ptr()] * world
+    s = torch.zeros(8, device="cuda").data_ptr()
     with pytest.raises(z.Zero1Error) as e:
         z.zero1_step_noalloc(n, world, z.Hparams(), 1, g, g, s, s, s)
     assert e.value.code == -1

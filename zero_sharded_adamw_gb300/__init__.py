@@ -174,15 +174,74 @@ class PtrTable:
     def __init__(self, xs):
         self.buffers = list(xs)
         self.array = (C.c_void_p * len(self.buffers))(*[_addr(x) for x in self.buffers])
+        self._checked: set = set()       # (count, kind, on_device) already validated
 
     def __len__(self) -> int:
         return len(self.buffers)
 
 
-def _ptrs(xs) -> C.Array:
+# Element kinds a C entry point expects behind a pointer: torch dtype name
+# and element size in bytes.
+_KINDS = {"bf16": ("torch.bfloat16", 2), "f32": ("torch.float32", 4)}
+
+
+def _check_buffer(x, count: int, kind: str, on_device: bool | None, what: str) -> None:
+    """Raise ValueError unless buffer `x` can hold `count` elements of `kind`
+    where the C side will look for them (on_device: True = CUDA memory,
+    False = host memory, None = either).  Raw integer addresses and None
+    pass unchecked: only objects that describe themselves can be checked."""
+    if x is None or isinstance(x, int):
+        return
+    want, size = _KINDS[kind]
+    if hasattr(x, "data_ptr") and hasattr(x, "numel"):          # torch tensor
+        if str(x.dtype) != want:
+            raise ValueError(f"{what}: expected {want}, got {x.dtype}")
+        if on_device is not None and bool(x.is_cuda) != on_device:
+            raise ValueError(f"{what}: expected a {'CUDA' if on_device else 'host'} tensor, got {x.device}")
+        if not x.is_contiguous():
+            raise ValueError(f"{what}: tensor is not contiguous")
+        if x.numel() < count:
+            raise ValueError(f"{what}: {x.numel()} elements, the call reads or writes {count}")
+    elif hasattr(x, "ctypes") and hasattr(x, "nbytes"):          # numpy array (host memory)
+        if on_device:
+            raise ValueError(f"{what}: a numpy array is host memory; this argument must be device memory")
+        if x.itemsize != size:
+            raise ValueError(f"{what}: {x.itemsize}-byte elements, expected {size}-byte {kind}")
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{what}: array is not contiguous")
+        if x.size < count:
+            raise ValueError(f"{what}: {x.size} elements, the call reads or writes {count}")
+
+
+def _ptrs(xs, world: int | None = None, count: int | None = None, kind: str | None = None,
+          on_device: bool | None = True, what: str = "buffers") -> C.Array:
+    """The host array of W pointers the C side reads.  With `world` it must
+    hold exactly W entries (the C side reads W of them); with `count` and
+    `kind` every buffer is checked to hold that many elements of that type."""
+    n = len(xs)
+    if world is not None and n != world:
+        raise ValueError(f"{what}: {n} pointers given, the call reads {world}")
     if isinstance(xs, PtrTable):
+        if count is not None and kind is not None:
+            key = (count, kind, on_device)
+            if key not in xs._checked:
+                for r, x in enumerate(xs.buffers):
+                    _check_buffer(x, count, kind, on_device, f"{what}[{r}]")
+                xs._checked.add(key)
         return xs.array
-    return (C.c_void_p * len(xs))(*[_addr(x) for x in xs])
+    if count is not None and kind is not None:
+        for r, x in enumerate(xs):
+            _check_buffer(x, count, kind, on_device, f"{what}[{r}]")
+    return (C.c_void_p * n)(*[_addr(x) for x in xs])
+
+
+# (n, world, moments in bf16) of every handle this binding created, so that
+# the per-call checks know the sizes the C side will use.
+_HANDLES: dict[int, tuple[int, int, bool]] = {}
+
+
+def _info(h) -> tuple[int | None, int | None, bool]:
+    return _HANDLES.get(h, (None, None, False))
 
 
 # --------------------------------------------------------- entry points
@@ -196,6 +255,7 @@ def zero1_create(n: int, world: int, hp: Hparams | None = None) -> int:
     h = C.c_void_p()
     c = (hp or Hparams())._c()
     _check(_load().zero1_create(n, world, C.byref(c), C.byref(h)))
+    _HANDLES[h.value] = (n, world, False)
     return h.value
 
 
@@ -205,47 +265,71 @@ def zero1_create_ex(n: int, world: int, hp: Hparams | None = None, opts: Options
     c = (hp or Hparams())._c()
     o = (opts or Options())._c()
     _check(_load().zero1_create_ex(n, world, C.byref(c), C.byref(o), C.byref(h)))
+    _HANDLES[h.value] = (n, world, bool(opts and opts.moments_bf16))
     return h.value
 
 
 def zero1_destroy(h: int | None) -> None:
     _check(_load().zero1_destroy(h))
+    _HANDLES.pop(h, None)
 
 
 def zero1_step(h: int, grad_ptrs, param_ptrs, stream=None) -> None:
     """One step: W device gradient buffers in, W device replicas out."""
-    _check(_load().zero1_step(h, _ptrs(grad_ptrs), _ptrs(param_ptrs), _stream(stream)))
+    n, world, _ = _info(h)
+    _check(_load().zero1_step(h, _ptrs(grad_ptrs, world, n, "bf16", True, "grads"),
+                              _ptrs(param_ptrs, world, n, "bf16", True, "params"), _stream(stream)))
 
 
 def zero1_step_host(h: int, host_grads, host_params, stream=None) -> None:
     """One step from host gradient buffers into host replica buffers (waits)."""
-    _check(_load().zero1_step_host(h, _ptrs(host_grads), _ptrs(host_params), _stream(stream)))
+    n, world, _ = _info(h)
+    _check(_load().zero1_step_host(h, _ptrs(host_grads, world, n, "bf16", False, "host_grads"),
+                                   _ptrs(host_params, world, n, "bf16", False, "host_params"), _stream(stream)))
 
 
 def zero1_step_host_async(h: int, host_grads, host_params, stream=None) -> None:
     """Pipelined host-buffer step; host_params are valid after zero1_host_sync."""
-    _check(_load().zero1_step_host_async(h, _ptrs(host_grads), _ptrs(host_params), _stream(stream)))
+    n, world, _ = _info(h)
+    _check(_load().zero1_step_host_async(h, _ptrs(host_grads, world, n, "bf16", False, "host_grads"),
+                                         _ptrs(host_params, world, n, "bf16", False, "host_params"),
+                                         _stream(stream)))
 
 
 def zero1_host_sync(h: int) -> None:
     _check(_load().zero1_host_sync(h))
 
 
+def _check_state(h, count, master, m, v) -> None:
+    """master fp32, m and v fp32 (bf16 on a moments_bf16 handle), each able
+    to hold `count` elements, in host or device memory."""
+    if count is None:
+        return
+    mom = "bf16" if _info(h)[2] else "f32"
+    _check_buffer(master, count, "f32", None, "master")
+    _check_buffer(m, count, mom, None, "m")
+    _check_buffer(v, count, mom, None, "v")
+
+
 def zero1_set_state(h: int, master, m=None, v=None, t: int = 0, stream=None) -> None:
+    _check_state(h, _info(h)[0], master, m, v)
     _check(_load().zero1_set_state(h, _addr(master), _addr(m), _addr(v), t, _stream(stream)))
 
 
 def zero1_get_state(h: int, master=None, m=None, v=None, stream=None) -> int:
+    _check_state(h, _info(h)[0], master, m, v)
     t = C.c_uint64()
     _check(_load().zero1_get_state(h, _addr(master), _addr(m), _addr(v), C.byref(t), _stream(stream)))
     return t.value
 
 
 def zero1_set_state_range(h: int, offset: int, count: int, master, m=None, v=None, stream=None) -> None:
+    _check_state(h, count, master, m, v)
     _check(_load().zero1_set_state_range(h, offset, count, _addr(master), _addr(m), _addr(v), _stream(stream)))
 
 
 def zero1_get_state_range(h: int, offset: int, count: int, master=None, m=None, v=None, stream=None) -> None:
+    _check_state(h, count, master, m, v)
     _check(_load().zero1_get_state_range(h, offset, count, _addr(master), _addr(m), _addr(v), _stream(stream)))
 
 
@@ -277,16 +361,22 @@ def zero1_bucket_begin(h: int) -> None:
 def zero1_bucket_reduce(h: int, offset: int, count: int, grad_ptrs, stream=None) -> None:
     """Reduce-scatter one bucket: grad_ptrs[r] holds rank r's gradient for
     parameters [offset, offset+count)."""
-    _check(_load().zero1_bucket_reduce(h, offset, count, _ptrs(grad_ptrs), _stream(stream)))
+    world = _info(h)[1]
+    _check(_load().zero1_bucket_reduce(h, offset, count, _ptrs(grad_ptrs, world, count, "bf16", True, "grads"),
+                                       _stream(stream)))
 
 
 def zero1_bucket_update(h: int, offset: int, count: int, grad_ptrs, param_ptrs, stream=None) -> None:
     """Reduce-scatter and update one bucket (handles without clipping)."""
-    _check(_load().zero1_bucket_update(h, offset, count, _ptrs(grad_ptrs), _ptrs(param_ptrs), _stream(stream)))
+    world = _info(h)[1]
+    _check(_load().zero1_bucket_update(h, offset, count, _ptrs(grad_ptrs, world, count, "bf16", True, "grads"),
+                                       _ptrs(param_ptrs, world, count, "bf16", True, "params"), _stream(stream)))
 
 
 def zero1_bucket_finish(h: int, param_ptrs, stream=None) -> None:
-    _check(_load().zero1_bucket_finish(h, None if param_ptrs is None else _ptrs(param_ptrs), _stream(stream)))
+    n, world, _ = _info(h)
+    table = None if param_ptrs is None else _ptrs(param_ptrs, world, n, "bf16", True, "params")
+    _check(_load().zero1_bucket_finish(h, table, _stream(stream)))
 
 
 def zero1_profile_start(h: int, capacity: int) -> None:
@@ -336,7 +426,11 @@ def zero1_step_noalloc(n: int, world: int, hp: Hparams, t: int, grad_ptrs, param
     """One step with caller-owned fp32 state and the library's fixed scratch
     (no device allocation; n <= 4,194,304)."""
     c = hp._c()
-    _check(_load().zero1_step_noalloc(n, world, C.byref(c), t, _ptrs(grad_ptrs), _ptrs(param_ptrs),
+    grads = _ptrs(grad_ptrs, world, n, "bf16", True, "grads")
+    params = _ptrs(param_ptrs, world, n, "bf16", True, "params")
+    for x, name in ((master, "master"), (m, "m"), (v, "v")):
+        _check_buffer(x, n, "f32", True, name)
+    _check(_load().zero1_step_noalloc(n, world, C.byref(c), t, grads, params,
                                       _addr(master), _addr(m), _addr(v), _stream(stream)))
 
 
@@ -346,14 +440,23 @@ OP_SUM, OP_AVG = 0, 1
 
 def zero1_allreduce(n: int, world: int, dtype: int, op: int, in_ptrs, out_ptrs, errors=None, stream=None) -> None:
     """DDP all-reduce of W device buffers (bf16 or fp32, sum or mean)."""
-    _check(_load().zero1_allreduce(n, world, dtype, op, _ptrs(in_ptrs), _ptrs(out_ptrs), _addr(errors),
+    kind = {DTYPE_BF16: "bf16", DTYPE_F32: "f32"}.get(dtype)
+    _check(_load().zero1_allreduce(n, world, dtype, op, _ptrs(in_ptrs, world, n, kind, True, "in"),
+                                   _ptrs(out_ptrs, world, n, kind, True, "out"), _addr(errors),
                                    _stream(stream)))
 
 
 def zero1_allgather(n: int, world: int, shard_len: int, dtype: int, shard_ptrs, out_ptrs, errors=None,
                     stream=None) -> None:
     """ZeRO-3 parameter all-gather: rank r's shard holds [r*S, min((r+1)*S, n))."""
-    _check(_load().zero1_allgather(n, world, shard_len, dtype, _ptrs(shard_ptrs), _ptrs(out_ptrs),
+    kind = {DTYPE_BF16: "bf16", DTYPE_F32: "f32"}.get(dtype)
+    shards = _ptrs(shard_ptrs, world, None, None, True, "shards")
+    if kind is not None and not isinstance(shard_ptrs, PtrTable):
+        for r, x in enumerate(shard_ptrs):
+            own = max(0, min(shard_len, n - r * shard_len))
+            if own:
+                _check_buffer(x, own, kind, True, f"shards[{r}]")
+    _check(_load().zero1_allgather(n, world, shard_len, dtype, shards, _ptrs(out_ptrs, world, n, kind, True, "out"),
                                    _addr(errors), _stream(stream)))
 
 

@@ -19,11 +19,22 @@
 // Host code must not hand the array's name to a kernel: on the host the
 // name is a stand-in, not a device address.  The first call on each device
 // (with that device current) looks the address up with cudaGetSymbolAddress
-// and caches it; that first call should therefore come before any stream
-// capture.  Every call shares the one array and its contents survive from
-// call to call, so the parts that must start at zero are cleared on the
-// stream at the start of each call; calls whose work overlaps on the GPU
-// (different streams, or different host threads) race on the array.
+// and caches it together with the identity of the CUDA context it was
+// looked up in; that first call should therefore come before any stream
+// capture.  Later calls compare the current context's identity with the
+// cached one (two driver queries, no device work) and look the address up
+// again when it changed, e.g. after cudaDeviceReset destroyed the context
+// and a new one loaded the module, possibly at another address.  Every call
+// shares the one array and its contents survive from call to call, so the
+// parts that must start at zero are cleared on the stream at the start of
+// each call; calls whose work overlaps on the GPU (different streams, or
+// different host threads) race on the array.
+//
+// The status block in the scratch also carries the sticky error bit that a
+// kernel pipeline wait sets when it gives up after its 1 s limit.  Each call
+// clears it with the rest of the status, and nothing on this path reads it
+// back, so such a timeout is not reported here (the handle-based step
+// reports it through zero1_get_grad_norm).
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -48,8 +59,45 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
+// Per device: the scratch address, the context it was looked up in
+// (cuCtxGetId's identity, unique for the life of the process) and the SM count.
 unsigned char *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
+
+// The two driver queries that identify the current context, fetched from the
+// driver through the runtime (the library does not link libcuda itself).
+// The handle types are opaque pointers; the return codes are CUresult,
+// where 0 is success.
+typedef int (*CtxGetCurrentFn)(void **ctx);
+typedef int (*CtxGetIdFn)(void *ctx, unsigned long long *id);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_ctx_fns_tried = false;
+
+// The identity of the calling thread's current context, or 0 if there is
+// none yet or the driver queries are unavailable (then the address is
+// looked up on every call).  Called with g_setup_mu held.
+unsigned long long current_context_id()
+{
+    if (!g_ctx_fns_tried) {
+        g_ctx_fns_tried = true;
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+        }
+    }
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    void *ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != 0 || ctx == nullptr || g_ctx_get_id(ctx, &id) != 0) return 0;
+    return id;
+}
 
 // Record the message for zero1_last_error() and return the code.
 int nfail(int code, const char *fmt, ...)
@@ -65,13 +113,14 @@ int nfail(int code, const char *fmt, ...)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Once per device, with that device current: the scratch's device address
-// and the SM count.
+// Once per device and context, with that device current: the scratch's
+// device address and the SM count.
 int setup_device(int dev, unsigned char **scratch, int *num_sms)
 {
     std::lock_guard<std::mutex> lk(g_setup_mu);
     if (dev < 0 || dev >= kMaxDevices) return nfail(ZERO1_ENODEV, "device ordinal %d out of range", dev);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         int major = 0, minor = 0, sms = 0;
         cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -85,6 +134,9 @@ int setup_device(int dev, unsigned char **scratch, int *num_sms)
             return nfail(ZERO1_ECUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
         g_scratch_addr[dev] = static_cast<unsigned char *>(addr);
         g_num_sms[dev] = sms;
+        // The lookup made the device's primary context current if no context
+        // was; record the context the address belongs to.
+        g_scratch_ctx[dev] = ctx != 0 ? ctx : current_context_id();
     }
     *scratch = g_scratch_addr[dev];
     *num_sms = g_num_sms[dev];

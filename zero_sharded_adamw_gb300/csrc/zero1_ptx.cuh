@@ -195,17 +195,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed()
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 
-// The double at the same shared-memory offset as `local`, in the CTA of
-// cluster rank `rank` (distributed shared memory).
-__device__ __forceinline__ double ld_cluster_f64(const double *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    double v;
-    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 // Store a double at the same shared-memory offset as `local`, in the CTA of
 // cluster rank `rank` (distributed shared memory).
 __device__ __forceinline__ void st_cluster_f64(double *local, uint32_t rank, double v)
