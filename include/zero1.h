@@ -138,6 +138,10 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     out after its 1 s limit; the step returns without hanging, and
  *     zero1_get_grad_norm then reports ZERO1_ECUDA (the sticky timeout bit).
  *     Applies to the two-kernel path (set small_step = -1 for small n).
+ *   host_chunk: parameters per chunk of the host-buffer steps
+ *     (zero1_step_host, zero1_step_host_async); 0 = the default, which makes
+ *     one ring slot (W ranks' bf16 slices of a chunk) 128 MiB.  Rounded down
+ *     to a multiple of 2048 (at least 2048); at most 65,536 chunks.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -148,6 +152,7 @@ typedef struct zero1_options {
     int32_t small_step;
     int32_t capturable;
     int32_t inject_wait_timeout;
+    uint64_t host_chunk;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).
@@ -184,15 +189,26 @@ int zero1_destroy(zero1_handle h);
 int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_ptrs, void *stream);
 
 /* The same step for callers whose gradients and replicas live in host
- * memory: copies the W host gradients to device staging buffers, runs
- * zero1_step, copies the W replicas back, and waits for the stream.
+ * memory, and waits for it: the W host gradients are uploaded, reduced,
+ * updated and the W replicas downloaded chunk by chunk (zero1_options
+ * host_chunk) through two bounded device rings, so the device memory the
+ * host path needs does not grow with n:
+ *   - rings: 2 x 4 slots of W x chunk bf16 (1 GiB at the default chunk);
+ *   - for W <= 2, an fp32 reduce-scatter scratch of 4*W*S bytes (the plain
+ *     step re-reads the gradients instead, which the host path cannot).
+ * Per step, every chunk is uploaded and reduce-scattered (with its norm
+ * partial) on an internal stream; after the last chunk the norm and clip
+ * coefficient are formed from the partials in chunk order, and every chunk
+ * is updated, cast, all-gathered into a download slot and copied back.
  *   host_grads:  W host pointers, n bf16 each (pinned memory recommended).
  *   host_params: W host pointers, n bf16 each, written.
- * The copies are cut into chunks of at most 64 MiB spread over four internal
- * copy streams (ordered after earlier work on `stream`, and `stream` waits
- * for them), so that several copy engines run at once.  The first call
- * allocates the staging buffers (4*W*n bytes) and creates those streams;
- * zero1_destroy frees both.  Errors as zero1_step, plus ZERO1_ENOMEM. */
+ * The step starts after earlier work on `stream`, and later work on
+ * `stream` starts after it.  The first call allocates the rings (and the
+ * W <= 2 scratch) and creates the internal streams and events;
+ * zero1_destroy frees them.  For a given clip coefficient the result equals
+ * zero1_step's bit for bit; the norm is summed in a chunking-dependent
+ * (fixed) order.  No profile events are recorded.  Refused while a
+ * bucketed step is open.  Errors as zero1_step, plus ZERO1_ENOMEM. */
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
 
 /* A ZeRO-2-style bucketed step ("Lecture 7 close reading", section 5.3:
@@ -239,20 +255,21 @@ int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const v
                         void *const *param_ptrs, void *stream);
 int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream);
 
-/* The host-buffer step, pipelined: enqueue and return.  Uploads this step's
- * gradients while the previous step's replicas are still downloading (the
- * two directions of the host link run at once), through two alternating
- * staging sets and separate upload and download copy streams.  Ordering:
- * the step runs on `stream` after the previous step; a staging set is
- * reused only after its last download finished.  The caller must keep
- * host_grads unchanged and must not read host_params until
+/* The host-buffer step, pipelined: enqueue and return.  The same chunked
+ * step as zero1_step_host, on the handle's internal streams: step t+1's
+ * chunk i is reduced as soon as step t's update of chunk i has read the
+ * scratch it overwrites, so one step's replica downloads overlap the next
+ * step's gradient uploads (the two directions of the host link run at
+ * once).  The step starts after earlier work on `stream`; any later call on
+ * the handle that touches its state (zero1_step, the state copies, the
+ * norm, the bucketed step) is ordered after it on that call's stream.  The
+ * caller must keep host_grads unchanged and must not read host_params until
  * zero1_host_sync(h) returns (host buffers may be the same every call).
- * The first call allocates 8*W*n bytes of staging and creates the streams;
- * zero1_destroy frees them.  Errors as zero1_step_host. */
+ * Errors as zero1_step_host. */
 int zero1_step_host_async(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream);
 
-/* Wait for every host-path copy of the handle (and so for the steps they
- * follow).  Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
+/* Wait for all work of the handle's host-buffer steps (copies and kernels).
+ * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
 int zero1_host_sync(zero1_handle h);
 
 /* Checkpoint restore ("Parallel training", "training loop and checkpoint":

@@ -136,7 +136,7 @@ def _struct_fields(name: str) -> list[tuple[str, str]]:
     return fields
 
 
-CTYPES = {"double": C.c_double, "uint32_t": C.c_uint32, "int32_t": C.c_int32}
+CTYPES = {"double": C.c_double, "uint32_t": C.c_uint32, "int32_t": C.c_int32, "uint64_t": C.c_uint64}
 
 
 @pytest.mark.parametrize("struct,binding", [("zero1_options", z._COptions), ("zero1_hparams", z._CHparams)])

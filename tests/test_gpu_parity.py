@@ -393,6 +393,81 @@ def test_step_host_async_matches_step_host():
     assert all(bits_equal(a, b) for a, b in zip(got_state[:3], want_state[:3]))
 
 
+@pytest.mark.parametrize("world", [2, 4])          # fp32 scratch kept by the handle (W >= 3) or by the host path
+def test_step_host_chunked_against_oracle_and_buckets(world):
+    """The host-buffer step cut into 16 chunks (the last one ragged): each
+    step is bit for bit the oracle's with the step's clip coefficient
+    injected, its norm within 1e-6 of the oracle's, and the result (norm
+    included) is the device bucketed step's with the same cut."""
+    n, chunk = 1_000_003, 65_536
+    w = WL.Workload(f"host_chunks_w{world}", n, world, 0.01, 3, max_norm=0.05)
+    zhp, ohp = _hp(w)
+    m0 = WL.master(w, "cuda")
+    cuts = [(lo, min(chunk, n - lo)) for lo in range(0, n, chunk)]
+    assert len(cuts) == 16
+    inj = o.State(f32(m0))
+    reps_d = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world, zhp, z.Options(host_chunk=chunk)) as a, z.Zero1(n, world, zhp) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, w.steps + 1):
+            g = WL.grads(w, t, "cuda")
+            hg = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True).copy_(x) for x in g]
+            hr = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+            a.step_host(hg, hr)
+            norm_a, c_a = a.grad_norm()
+            z.zero1_bucket_begin(b.handle)
+            for lo, cnt in cuts:
+                z.zero1_bucket_reduce(b.handle, lo, cnt, [x[lo:lo + cnt] for x in g])
+            z.zero1_bucket_finish(b.handle, reps_d)
+            norm_b, c_b = b.grad_norm()
+            assert norm_a == norm_b and c_a == c_b, (t, norm_a, norm_b)
+            reps_i, norm_i, _ = o.step(inj, [u16(x) for x in g], ohp, clip_override=np.float32(c_a))
+            assert abs(norm_a - norm_i) <= TOL * norm_i
+            sa, sb = _state(a, n), _state(b, n)
+            assert sa[3] == sb[3] == t
+            for x, y, ref in zip(sa[:3], sb[:3], (inj.master, inj.m, inj.v)):
+                assert bits_equal(x, ref) and bits_equal(y, ref), t
+            for r in range(world):
+                assert np.array_equal(u16(hr[r]), reps_i[r]), (t, r)
+                assert np.array_equal(u16(reps_d[r]), reps_i[r]), (t, r)
+
+
+def test_step_host_async_chunked_pipelined():
+    """Six pipelined host-buffer steps over 16 chunks (step t's downloads
+    overlap step t+1's uploads) equal six blocking ones bit for bit, each
+    step's replicas in its own host buffers; a device step enqueued right
+    after them without zero1_host_sync is ordered after them; a capturable
+    handle's device step counter advances once per step."""
+    n, world, chunk, steps = 1_000_003, 4, 65_536, 6
+    w = WL.Workload("host_pipe", n, world, 0.01, steps, max_norm=0.05)
+    zhp, _ = _hp(w)
+    m0 = WL.master(w, "cuda")
+    hgs = [[torch.empty(n, dtype=torch.bfloat16, pin_memory=True).copy_(x) for x in WL.grads(w, t, "cuda")]
+           for t in range(1, steps + 1)]
+    g_last = WL.grads(w, steps + 1, "cuda")
+    fresh = lambda: [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+    results = []
+    for capturable, pipelined in ((False, False), (False, True), (True, True)):
+        outs = [fresh() for _ in range(steps)]
+        reps = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+        with z.Zero1(n, world, zhp, z.Options(host_chunk=chunk, capturable=capturable)) as opt:
+            opt.set_state(m0)
+            for t in range(steps):
+                (opt.step_host_async if pipelined else opt.step_host)(hgs[t], outs[t])
+            opt.step(g_last, reps)             # ordered after the host steps by the handle itself
+            st = _state(opt, n)
+            opt.host_sync()
+            assert st[3] == steps + 1
+            results.append(([[u16(r) for r in out] for out in outs], st, [u16(r) for r in reps]))
+    (outs0, st0, reps0) = results[0]
+    for outs, st, reps in results[1:]:
+        for t in range(steps):
+            assert all(np.array_equal(a, b) for a, b in zip(outs[t], outs0[t])), t
+        assert all(bits_equal(a, b) for a, b in zip(st[:3], st0[:3]))
+        assert all(np.array_equal(a, b) for a, b in zip(reps, reps0))
+
+
 # --------------------------------------------------------- full sizes
 
 def _windows(n: int, world: int, shard: int, rng, width=4096, n_random=8):

@@ -18,7 +18,7 @@ import os
 from dataclasses import dataclass
 
 __all__ = [
-    "Zero1Error", "Hparams", "Options", "Zero1", "PtrTable",
+    "Zero1Error", "Zero1ArgumentError", "Hparams", "Options", "Zero1", "PtrTable",
     "zero1_create", "zero1_create_ex", "zero1_destroy", "zero1_step", "zero1_step_host",
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
@@ -75,6 +75,15 @@ class Zero1Error(RuntimeError):
         self.code = code
 
 
+class Zero1ArgumentError(Zero1Error, ValueError):
+    """An argument the binding refused before calling the library (a pointer
+    list whose length is not the world size, a buffer of the wrong type,
+    place or size): code ZERO1_EINVAL, like the library's own checks."""
+
+    def __init__(self, message: str):
+        super().__init__(-1, message)
+
+
 class _CHparams(C.Structure):
     _fields_ = [(k, C.c_double) for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_norm")]
 
@@ -96,7 +105,7 @@ class Hparams:
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
                 ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32),
-                ("capturable", C.c_int32), ("inject_wait_timeout", C.c_int32)]
+                ("capturable", C.c_int32), ("inject_wait_timeout", C.c_int32), ("host_chunk", C.c_uint64)]
 
 
 @dataclass
@@ -104,7 +113,8 @@ class Options:
     """Step variants: torch.optim.AdamW's decay order, a clip eps (torch's
     clip_grad_norm_ uses 1e-6), m and v stored in bf16; the bucketed step's
     CTAs per bucket; the one-launch small-n path (0 auto, 1 on, -1 off);
-    capturable steps (device-side step counter and lr, for CUDA graphs)."""
+    capturable steps (device-side step counter and lr, for CUDA graphs);
+    the host-buffer steps' chunk size."""
     decay_before_update: bool = False
     clip_eps: float = 0.0
     moments_bf16: bool = False
@@ -112,11 +122,12 @@ class Options:
     small_step: int = 0
     capturable: bool = False
     inject_wait_timeout: bool = False    # failure testing: the update kernel's waits run out
+    host_chunk: int = 0                  # host-buffer steps: parameters per chunk (0 = default)
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
                          1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step,
-                         1 if self.capturable else 0, 1 if self.inject_wait_timeout else 0)
+                         1 if self.capturable else 0, 1 if self.inject_wait_timeout else 0, self.host_chunk)
 
 
 _lib = None
@@ -195,22 +206,22 @@ def _check_buffer(x, count: int, kind: str, on_device: bool | None, what: str) -
     want, size = _KINDS[kind]
     if hasattr(x, "data_ptr") and hasattr(x, "numel"):          # torch tensor
         if str(x.dtype) != want:
-            raise ValueError(f"{what}: expected {want}, got {x.dtype}")
+            raise Zero1ArgumentError(f"{what}: expected {want}, got {x.dtype}")
         if on_device is not None and bool(x.is_cuda) != on_device:
-            raise ValueError(f"{what}: expected a {'CUDA' if on_device else 'host'} tensor, got {x.device}")
+            raise Zero1ArgumentError(f"{what}: expected a {'CUDA' if on_device else 'host'} tensor, got {x.device}")
         if not x.is_contiguous():
-            raise ValueError(f"{what}: tensor is not contiguous")
+            raise Zero1ArgumentError(f"{what}: tensor is not contiguous")
         if x.numel() < count:
-            raise ValueError(f"{what}: {x.numel()} elements, the call reads or writes {count}")
+            raise Zero1ArgumentError(f"{what}: {x.numel()} elements, the call reads or writes {count}")
     elif hasattr(x, "ctypes") and hasattr(x, "nbytes"):          # numpy array (host memory)
         if on_device:
-            raise ValueError(f"{what}: a numpy array is host memory; this argument must be device memory")
+            raise Zero1ArgumentError(f"{what}: a numpy array is host memory; this argument must be device memory")
         if x.itemsize != size:
-            raise ValueError(f"{what}: {x.itemsize}-byte elements, expected {size}-byte {kind}")
+            raise Zero1ArgumentError(f"{what}: {x.itemsize}-byte elements, expected {size}-byte {kind}")
         if not x.flags["C_CONTIGUOUS"]:
-            raise ValueError(f"{what}: array is not contiguous")
+            raise Zero1ArgumentError(f"{what}: array is not contiguous")
         if x.size < count:
-            raise ValueError(f"{what}: {x.size} elements, the call reads or writes {count}")
+            raise Zero1ArgumentError(f"{what}: {x.size} elements, the call reads or writes {count}")
 
 
 def _ptrs(xs, world: int | None = None, count: int | None = None, kind: str | None = None,
@@ -220,7 +231,7 @@ def _ptrs(xs, world: int | None = None, count: int | None = None, kind: str | No
     `kind` every buffer is checked to hold that many elements of that type."""
     n = len(xs)
     if world is not None and n != world:
-        raise ValueError(f"{what}: {n} pointers given, the call reads {world}")
+        raise Zero1ArgumentError(f"{what}: {n} pointers given, the call reads {world}")
     if isinstance(xs, PtrTable):
         if count is not None and kind is not None:
             key = (count, kind, on_device)

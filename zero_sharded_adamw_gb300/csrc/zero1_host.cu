@@ -29,11 +29,41 @@
 #include "zero1.h"
 #include "zero1_internal.h"
 
-// A set of copy streams that host<->device copies are dealt over.
-struct CopyLanes {
+// Slots in each of the host path's two device rings (uploads, downloads).
+constexpr int kHostSlots = 4;
+// Device bytes of one slot by default: the W ranks' bf16 slices of one chunk.
+constexpr uint64_t kHostSlotBytes = 128ull << 20;
+constexpr uint64_t kHostChunkAlign = 2048;   // chunks start on whole update tiles
+
+// The host-buffer steps (zero1_step_host, zero1_step_host_async): gradients
+// and replicas live in host memory and pass through two bounded device rings
+// chunk by chunk.  Per step, every chunk's W gradient slices are uploaded
+// into a ring slot and reduce-scattered into the fp32 scratch (with the
+// chunk's norm partial) on the reduce stream; once the last chunk's partial
+// is in, the update stream runs each chunk's clip + AdamW + bf16 cast +
+// all-gather into a download slot, which a download stream copies to the W
+// host replicas.  Step t+1's chunk i reduce waits only for step t's chunk i
+// update (the scratch it overwrites), so one step's downloads overlap the
+// next step's uploads.  The norm partials alternate between two sets by
+// step parity, since step t's updates still read step t's set while step
+// t+1's reduces fill the other.
+struct HostPath {
     bool ready = false;
-    cudaStream_t s[4] = {};
-    cudaEvent_t fork = nullptr, join[4] = {};
+    uint64_t chunk = 0;            // parameters per chunk (a multiple of kHostChunkAlign)
+    int nchunks = 0;
+    uint64_t rank_stride = 0;      // bytes between ranks' slices in a slot (256-byte rounded)
+    void *staging = nullptr;       // kHostSlots upload slots, then kHostSlots download slots
+    double *sums = nullptr;        // 2 parity sets x nchunks x (sum, plain sum)
+    cudaStream_t rs = nullptr, upd = nullptr, up[2] = {}, down[2] = {};
+    cudaEvent_t fork = nullptr, norm_done = nullptr, last = nullptr;
+    cudaEvent_t up_ready[kHostSlots] = {}, up_free[kHostSlots] = {};
+    cudaEvent_t down_ready[kHostSlots] = {}, down_free[kHostSlots] = {};
+    bool up_used[kHostSlots] = {}, down_used[kHostSlots] = {};
+    std::vector<cudaEvent_t> upd_done;   // per chunk: the latest step's update of it has read the scratch
+    std::vector<char> upd_recorded;
+    uint64_t up_count = 0, down_count = 0;
+    int parity = 0;
+    bool pending = false;          // steps enqueued on the internal streams and not yet joined
 };
 
 struct zero1_ctx {
@@ -55,28 +85,20 @@ struct zero1_ctx {
     size_t msz = sizeof(float);
     double *partials = nullptr;
     zero1::DevStatus *status = nullptr;
-    // host-path staging (zero1_step_host), allocated on first use, and the
-    // copy streams its host<->device copies are spread over
-    void *staging = nullptr;
-    uint64_t staging_stride = 0;
-    CopyLanes copy;
+    // host-buffer steps (zero1_step_host, zero1_step_host_async): rings,
+    // streams and events, set up on first use
+    HostPath host;
     // capturable handles: bias-correction table (1 - beta1^t, 1 - beta2^t)
     // for t = 1..tab_len on the device, and where the kernels read lr
     double2 *bctab = nullptr;
     uint64_t tab_len = 0;
     const double *lr_ptr = nullptr;
-    // pipelined host path (zero1_step_host_async): two staging sets, upload
-    // and download lanes, and per set the events its last download recorded
-    void *astaging = nullptr;
-    int aset = 0;
-    bool aused[2] = {false, false};
-    CopyLanes up, down;
-    cudaEvent_t afree[2][4] = {};
     // per-kernel timing (zero1_profile_start/stop): 3 events per step
     std::vector<cudaEvent_t> prof;
     int prof_capacity = 0, prof_used = 0;
     // bucketed step (zero1_bucket_*): buckets in call order, their norm sums,
-    // and a reduce-scatter scratch for W <= 2 (whose plain step re-reads)
+    // and a reduce-scatter scratch for W <= 2 (whose plain step re-reads;
+    // the host-buffer steps use it too)
     bool bucket_open = false;
     int bucket_mode = 0;         // 0: no bucket yet, 1: reduce-only buckets, 2: reduce + update buckets
     std::vector<std::pair<uint64_t, uint64_t>> buckets;
@@ -199,6 +221,31 @@ struct DeviceGuard {
         if (prev >= 0) cudaSetDevice(prev);
     }
 };
+
+// Work a host-buffer step left on the handle's internal streams comes
+// before anything the caller enqueues on `st` afterwards (the steps share
+// the state, the scratch and the status).
+int join_host(zero1_ctx *h, cudaStream_t st)
+{
+    if (!h->host.pending) return ZERO1_OK;
+    cudaError_t e = cudaStreamWaitEvent(st, h->host.last, 0);
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e, "cudaStreamWaitEvent");
+}
+
+void release_host_path(HostPath &P)
+{
+    for (cudaStream_t x : {P.rs, P.upd, P.up[0], P.up[1], P.down[0], P.down[1]})
+        if (x) cudaStreamDestroy(x);
+    for (cudaEvent_t x : {P.fork, P.norm_done, P.last})
+        if (x) cudaEventDestroy(x);
+    for (int i = 0; i < kHostSlots; ++i)
+        for (cudaEvent_t x : {P.up_ready[i], P.up_free[i], P.down_ready[i], P.down_free[i]})
+            if (x) cudaEventDestroy(x);
+    for (cudaEvent_t x : P.upd_done)
+        if (x) cudaEventDestroy(x);
+    if (P.sums) cudaFree(P.sums);
+    P = HostPath{};
+}
 
 }  // namespace
 
@@ -372,22 +419,11 @@ int zero1_destroy(zero1_handle h)
     DeviceGuard g(h->device);
     cudaError_t e1 = cudaDeviceSynchronize();
     cudaError_t e2 = cudaFree(h->block);
-    cudaError_t e3 = h->staging ? cudaFree(h->staging) : cudaSuccess;
+    cudaError_t e3 = h->host.staging ? cudaFree(h->host.staging) : cudaSuccess;
     if (h->bucket_sums) cudaFree(h->bucket_sums);
     if (h->ghat_bucket) cudaFree(h->ghat_bucket);
     for (cudaEvent_t ev : h->prof) cudaEventDestroy(ev);
-    for (CopyLanes *l : {&h->copy, &h->up, &h->down}) {
-        if (!l->ready) continue;
-        for (int i = 0; i < 4; ++i) {
-            cudaStreamDestroy(l->s[i]);
-            cudaEventDestroy(l->join[i]);
-        }
-        cudaEventDestroy(l->fork);
-    }
-    for (auto &set : h->afree)
-        for (cudaEvent_t ev : set)
-            if (ev) cudaEventDestroy(ev);
-    if (h->astaging) cudaFree(h->astaging);
+    release_host_path(h->host);
     if (h->bctab) cudaFree(h->bctab);
     delete h;
     if (e1 != cudaSuccess) return cuda_fail(e1, "cudaDeviceSynchronize in destroy");
@@ -407,6 +443,8 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
             return fail(ZERO1_EALIGN, "rank %d buffer is not 16-byte aligned", r);
     }
     DeviceGuard g(h->device);
+    int rc = join_host(h, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
     zero1::StepLaunch s;
     s.grads = grad_ptrs;
     s.params = param_ptrs;
@@ -439,56 +477,217 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
 
 namespace {
 
-constexpr int kCopyStreams = 4;
-constexpr uint64_t kCopyChunk = 64ull << 20;
-
-// Create a lane set's streams and events on first use.
-int lanes_ready(CopyLanes &l)
+// The reduce-scatter + norm partial of parameters [offset, offset+count)
+// (the reduce kernel in bucket mode): the gradients come from grad_ptrs,
+// whose entries point at that range; the fp32 result goes to ghat + offset
+// and the range's partial (sum, plain sum) to sums[2*index].  max_ctas > 0
+// caps the grid.
+int launch_rs_piece(zero1_ctx *h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, float *ghat,
+                    double *sums, int index, int max_ctas, cudaStream_t st)
 {
-    if (l.ready) return ZERO1_OK;
+    zero1::StepLaunch s;
+    s.grads = grad_ptrs;
+    s.params = nullptr;
+    s.world = h->world;
+    s.n = count;
+    s.master = h->master;
+    s.m = h->m;
+    s.v = h->v;
+    s.ghat = ghat + offset;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = launch_scalars(h, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    s.clip_eps = h->opts.clip_eps;
+    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    if (max_ctas > 0 && s.grid_rs > max_ctas) s.grid_rs = max_ctas;
+    s.phase = 1;
+    s.bucket_sums = sums;
+    s.bucket_index = index;
+    cudaError_t e = zero1::launch_step(s, st, nullptr);
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e, "kernel launch");
+}
+
+// The clip + AdamW + bf16 cast + all-gather of parameters [offset,
+// offset+count) (the update kernel, c formed from the first nsums norm
+// partials in order): the replicas go to param_ptrs, whose entries point at
+// that range.  capturable: the step scalars come from the device counter,
+// which this launch advances only if advance_t.
+int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *const *param_ptrs, float *ghat,
+                        double *sums, int nsums, bool capturable, bool advance_t, int max_ctas, cudaStream_t st)
+{
+    zero1::StepLaunch s;
+    s.grads = nullptr;
+    s.params = param_ptrs;
+    s.world = h->world;
+    s.n = count;
+    s.master = h->master + offset;
+    s.m = h->m + offset * h->msz;
+    s.v = h->v + offset * h->msz;
+    s.ghat = ghat + offset;
+    s.partials = h->partials;
+    s.status = h->status;
+    s.sc = launch_scalars(h, h->t + 1);
+    s.max_norm = h->hp.max_norm;
+    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    if (max_ctas > 0 && s.grid_update > max_ctas) s.grid_update = max_ctas;
+    s.moments_bf16 = h->opts.moments_bf16 != 0;
+    s.decay_first = h->opts.decay_before_update != 0;
+    s.clip_eps = h->opts.clip_eps;
+    s.phase = 2;
+    s.bucket_sums = sums;
+    s.nbuckets = nsums;
+    if (capturable) s.dev = dev_scalars(h);
+    s.advance_t = advance_t;
+    cudaError_t e = zero1::launch_step(s, st, nullptr);
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e, "kernel launch");
+}
+
+constexpr uint64_t kHostMaxChunks = 1ull << 16;
+
+// Rings, streams and events of the host-buffer steps, on first use.
+int host_path_ready(zero1_ctx *h)
+{
+    HostPath &P = h->host;
+    if (P.ready) return ZERO1_OK;
+    uint64_t chunk = h->opts.host_chunk;
+    if (chunk == 0) chunk = kHostSlotBytes / (2ull * (uint64_t)h->world);
+    chunk = std::max<uint64_t>(kHostChunkAlign, chunk / kHostChunkAlign * kHostChunkAlign);
+    chunk = std::min<uint64_t>(chunk, round_up(h->n, kHostChunkAlign));
+    const uint64_t nchunks = (h->n + chunk - 1) / chunk;
+    if (nchunks > kHostMaxChunks)
+        return fail(ZERO1_EINVAL, "host_chunk %llu cuts n into %llu chunks (at most %llu)",
+                    (unsigned long long)chunk, (unsigned long long)nchunks, (unsigned long long)kHostMaxChunks);
     cudaError_t e;
-    for (int i = 0; i < kCopyStreams; ++i) {
-        if ((e = cudaStreamCreateWithFlags(&l.s[i], cudaStreamNonBlocking)) != cudaSuccess)
-            return cuda_fail(e, "cudaStreamCreate");
-        if ((e = cudaEventCreateWithFlags(&l.join[i], cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_fail(e, "cudaEventCreate");
+    // W <= 2: the fp32 reduce-scatter scratch the plain step does without.
+    if (!h->ghat && !h->ghat_bucket &&
+        (e = cudaMalloc(&h->ghat_bucket, round_up(h->padded * sizeof(float), 256))) != cudaSuccess) {
+        h->ghat_bucket = nullptr;
+        return cuda_fail(e, "cudaMalloc of the reduce-scatter scratch");
     }
-    if ((e = cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming)) != cudaSuccess)
-        return cuda_fail(e, "cudaEventCreate");
-    l.ready = true;
+    HostPath Q;
+    Q.chunk = chunk;
+    Q.nchunks = (int)nchunks;
+    Q.rank_stride = round_up(chunk * 2, 256);
+    const uint64_t slot_bytes = Q.rank_stride * (uint64_t)h->world;
+    auto undo = [&](cudaError_t err, const char *what) {
+        if (Q.staging) cudaFree(Q.staging);
+        release_host_path(Q);
+        return cuda_fail(err, what);
+    };
+    if ((e = cudaMalloc(&Q.staging, 2 * kHostSlots * slot_bytes)) != cudaSuccess) {
+        Q.staging = nullptr;
+        return undo(e, "cudaMalloc of the host-path rings");
+    }
+    if ((e = cudaMalloc(&Q.sums, 4 * nchunks * sizeof(double))) != cudaSuccess) {
+        Q.sums = nullptr;
+        return undo(e, "cudaMalloc of the host-path norm partials");
+    }
+    for (cudaStream_t *x : {&Q.rs, &Q.upd, &Q.up[0], &Q.up[1], &Q.down[0], &Q.down[1]})
+        if ((e = cudaStreamCreateWithFlags(x, cudaStreamNonBlocking)) != cudaSuccess) return undo(e, "cudaStreamCreate");
+    std::vector<cudaEvent_t *> evs = {&Q.fork, &Q.norm_done, &Q.last};
+    for (int i = 0; i < kHostSlots; ++i)
+        for (cudaEvent_t *x : {&Q.up_ready[i], &Q.up_free[i], &Q.down_ready[i], &Q.down_free[i]}) evs.push_back(x);
+    Q.upd_done.assign(nchunks, nullptr);
+    for (auto &x : Q.upd_done) evs.push_back(&x);
+    for (cudaEvent_t *x : evs)
+        if ((e = cudaEventCreateWithFlags(x, cudaEventDisableTiming)) != cudaSuccess) return undo(e, "cudaEventCreate");
+    Q.upd_recorded.assign(nchunks, 0);
+    Q.ready = true;
+    P = std::move(Q);
     return ZERO1_OK;
 }
 
-// `count` copies of `bytes` each, cut into chunks of at most 64 MiB and dealt
-// round-robin over the lanes so that several copy engines run at once; they
-// start after the work already on `st`.  With join_back, the work enqueued
-// on `st` afterwards waits for all of them; either way l.join[i] marks the
-// end of lane i's part.
-int spread_copies(CopyLanes &l, void *const *dst, const void *const *src, int count, uint64_t bytes,
-                  cudaMemcpyKind kind, cudaStream_t st, bool join_back)
+#define HOST_CHECK(call, what)                              \
+    do {                                                    \
+        cudaError_t err_ = (call);                          \
+        if (err_ != cudaSuccess) return cuda_fail(err_, what); \
+    } while (0)
+
+// One host-buffer step: enqueue every chunk's upload, reduce, update and
+// download on the handle's internal streams (see HostPath).  blocking:
+// wait for all of it before returning.
+int host_step(zero1_ctx *h, const void *const *host_grads, void *const *host_params, cudaStream_t st, bool blocking)
 {
-    int rc = lanes_ready(l);
+    int rc = host_path_ready(h);
     if (rc) return rc;
-    cudaError_t e;
-    if ((e = cudaEventRecord(l.fork, st)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    for (int i = 0; i < kCopyStreams; ++i)
-        if ((e = cudaStreamWaitEvent(l.s[i], l.fork, 0)) != cudaSuccess)
-            return cuda_fail(e, "cudaStreamWaitEvent");
-    int next = 0;
-    for (int r = 0; r < count; ++r) {
-        for (uint64_t off = 0; off < bytes; off += kCopyChunk) {
-            const uint64_t len = bytes - off < kCopyChunk ? bytes - off : kCopyChunk;
-            e = cudaMemcpyAsync(static_cast<char *>(dst[r]) + off, static_cast<const char *>(src[r]) + off, len,
-                                kind, l.s[next]);
-            if (e != cudaSuccess) return cuda_fail(e, "host/device copy");
-            next = (next + 1) % kCopyStreams;
+    HostPath &P = h->host;
+    const int W = h->world, M = P.nchunks;
+    const bool capturable = h->bctab != nullptr;
+    float *ghat = h->ghat ? h->ghat : h->ghat_bucket;
+    double *sums = P.sums + (size_t)P.parity * 2 * (size_t)M;
+    char *ring = static_cast<char *>(P.staging);
+    const uint64_t slot_bytes = P.rank_stride * (uint64_t)W;
+    const void *gslot[ZERO1_MAX_WORLD];
+    void *pslot[ZERO1_MAX_WORLD];
+
+    // The step follows the caller's earlier work on `st`.
+    HOST_CHECK(cudaEventRecord(P.fork, st), "cudaEventRecord");
+    HOST_CHECK(cudaStreamWaitEvent(P.rs, P.fork, 0), "cudaStreamWaitEvent");
+    for (int i = 0; i < M; ++i) {                    // uploads and reduces
+        const uint64_t lo = (uint64_t)i * P.chunk, cnt = std::min<uint64_t>(P.chunk, h->n - lo);
+        const int sl = (int)(P.up_count % kHostSlots);
+        cudaStream_t u = P.up[P.up_count % 2];
+        char *base = ring + (uint64_t)sl * slot_bytes;
+        if (P.up_used[sl]) HOST_CHECK(cudaStreamWaitEvent(u, P.up_free[sl], 0), "cudaStreamWaitEvent");
+        for (int r = 0; r < W; ++r) {
+            void *dst = base + (uint64_t)r * P.rank_stride;
+            gslot[r] = dst;
+            HOST_CHECK(cudaMemcpyAsync(dst, static_cast<const char *>(host_grads[r]) + lo * 2, cnt * 2,
+                                       cudaMemcpyHostToDevice, u),
+                       "gradient upload");
         }
+        HOST_CHECK(cudaEventRecord(P.up_ready[sl], u), "cudaEventRecord");
+        HOST_CHECK(cudaStreamWaitEvent(P.rs, P.up_ready[sl], 0), "cudaStreamWaitEvent");
+        // the previous step's update of this chunk has read the scratch it overwrites
+        if (P.upd_recorded[i]) HOST_CHECK(cudaStreamWaitEvent(P.rs, P.upd_done[i], 0), "cudaStreamWaitEvent");
+        if ((rc = launch_rs_piece(h, lo, cnt, gslot, ghat, sums, i, 0, P.rs))) return rc;
+        HOST_CHECK(cudaEventRecord(P.up_free[sl], P.rs), "cudaEventRecord");
+        P.up_used[sl] = true;
+        ++P.up_count;
     }
-    for (int i = 0; i < kCopyStreams; ++i) {
-        if ((e = cudaEventRecord(l.join[i], l.s[i])) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if (join_back && (e = cudaStreamWaitEvent(st, l.join[i], 0)) != cudaSuccess)
-            return cuda_fail(e, "cudaStreamWaitEvent");
+    HOST_CHECK(cudaEventRecord(P.norm_done, P.rs), "cudaEventRecord");
+    HOST_CHECK(cudaStreamWaitEvent(P.upd, P.norm_done, 0), "cudaStreamWaitEvent");
+    for (int i = 0; i < M; ++i) {                    // updates and downloads
+        const uint64_t lo = (uint64_t)i * P.chunk, cnt = std::min<uint64_t>(P.chunk, h->n - lo);
+        const int sl = (int)(P.down_count % kHostSlots);
+        cudaStream_t d = P.down[P.down_count % 2];
+        char *base = ring + (uint64_t)(kHostSlots + sl) * slot_bytes;
+        if (P.down_used[sl]) HOST_CHECK(cudaStreamWaitEvent(P.upd, P.down_free[sl], 0), "cudaStreamWaitEvent");
+        for (int r = 0; r < W; ++r) pslot[r] = base + (uint64_t)r * P.rank_stride;
+        if ((rc = launch_update_piece(h, lo, cnt, pslot, ghat, sums, M, capturable, i == M - 1, 0, P.upd)))
+            return rc;
+        HOST_CHECK(cudaEventRecord(P.upd_done[i], P.upd), "cudaEventRecord");
+        P.upd_recorded[i] = 1;
+        HOST_CHECK(cudaEventRecord(P.down_ready[sl], P.upd), "cudaEventRecord");
+        HOST_CHECK(cudaStreamWaitEvent(d, P.down_ready[sl], 0), "cudaStreamWaitEvent");
+        for (int r = 0; r < W; ++r)
+            HOST_CHECK(cudaMemcpyAsync(static_cast<char *>(host_params[r]) + lo * 2, pslot[r], cnt * 2,
+                                       cudaMemcpyDeviceToHost, d),
+                       "replica download");
+        HOST_CHECK(cudaEventRecord(P.down_free[sl], d), "cudaEventRecord");
+        P.down_used[sl] = true;
+        ++P.down_count;
     }
+    HOST_CHECK(cudaEventRecord(P.last, P.upd), "cudaEventRecord");
+    P.parity ^= 1;
+    P.pending = true;
+    h->t += 1;
+    if (blocking) {
+        HOST_CHECK(cudaStreamWaitEvent(st, P.last, 0), "cudaStreamWaitEvent");
+        for (cudaStream_t x : {P.upd, P.down[0], P.down[1]})
+            HOST_CHECK(cudaStreamSynchronize(x), "cudaStreamSynchronize");
+        P.pending = false;
+    }
+    return ZERO1_OK;
+}
+
+int check_host_call(zero1_ctx *h, const void *const *host_grads, void *const *host_params)
+{
+    if (h->bucket_open) return fail(ZERO1_EINVAL, "a bucketed step is open; finish it first");
+    if (!host_grads || !host_params) return fail(ZERO1_EINVAL, "pointer array is NULL");
+    for (int r = 0; r < h->world; ++r)
+        if (!host_grads[r] || !host_params[r]) return fail(ZERO1_EINVAL, "rank %d host buffer is NULL", r);
     return ZERO1_OK;
 }
 
@@ -497,98 +696,32 @@ int spread_copies(CopyLanes &l, void *const *dst, const void *const *src, int co
 int zero1_step_host(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
-    if (!host_grads || !host_params) return fail(ZERO1_EINVAL, "pointer array is NULL");
-    for (int r = 0; r < h->world; ++r)
-        if (!host_grads[r] || !host_params[r]) return fail(ZERO1_EINVAL, "rank %d host buffer is NULL", r);
+    int rc = check_host_call(h, host_grads, host_params);
+    if (rc) return rc;
     DeviceGuard g(h->device);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint64_t bytes = h->n * 2;
-    cudaError_t e;
-    if (!h->staging) {
-        h->staging_stride = round_up(bytes, 256);
-        if ((e = cudaMalloc(&h->staging, 2 * (uint64_t)h->world * h->staging_stride)) != cudaSuccess) {
-            h->staging = nullptr;
-            return cuda_fail(e, "cudaMalloc of staging buffers");
-        }
-    }
-    void *dg[ZERO1_MAX_WORLD];
-    void *dp[ZERO1_MAX_WORLD];
-    char *base = static_cast<char *>(h->staging);
-    for (int r = 0; r < h->world; ++r) {
-        dg[r] = base + (uint64_t)r * h->staging_stride;
-        dp[r] = base + (uint64_t)(h->world + r) * h->staging_stride;
-    }
-    int rc = spread_copies(h->copy, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st, true);
-    if (rc) return rc;
-    rc = zero1_step(h, dg, dp, stream);
-    if (rc) return rc;
-    rc = spread_copies(h->copy, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st, true);
-    if (rc) return rc;
-    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    return ZERO1_OK;
+    return host_step(h, host_grads, host_params, static_cast<cudaStream_t>(stream), true);
 }
 
 int zero1_step_host_async(zero1_handle h, const void *const *host_grads, void *const *host_params, void *stream)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
-    if (!host_grads || !host_params) return fail(ZERO1_EINVAL, "pointer array is NULL");
-    for (int r = 0; r < h->world; ++r)
-        if (!host_grads[r] || !host_params[r]) return fail(ZERO1_EINVAL, "rank %d host buffer is NULL", r);
+    int rc = check_host_call(h, host_grads, host_params);
+    if (rc) return rc;
     DeviceGuard g(h->device);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint64_t bytes = h->n * 2;
-    const uint64_t stride = round_up(bytes, 256);
-    cudaError_t e;
-    if (!h->astaging) {
-        if ((e = cudaMalloc(&h->astaging, 4 * (uint64_t)h->world * stride)) != cudaSuccess) {
-            h->astaging = nullptr;
-            return cuda_fail(e, "cudaMalloc of staging buffers");
-        }
-        for (auto &set : h->afree)
-            for (cudaEvent_t &ev : set)
-                if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
-                    return cuda_fail(e, "cudaEventCreate");
-    }
-    int rc;
-    if ((rc = lanes_ready(h->up)) || (rc = lanes_ready(h->down))) return rc;
-    const int set = h->aset;
-    void *dg[ZERO1_MAX_WORLD];
-    void *dp[ZERO1_MAX_WORLD];
-    char *base = static_cast<char *>(h->astaging) + (uint64_t)set * 2 * h->world * stride;
-    for (int r = 0; r < h->world; ++r) {
-        dg[r] = base + (uint64_t)r * stride;
-        dp[r] = base + (uint64_t)(h->world + r) * stride;
-    }
-    // This staging set is free once the download that last read it is done.
-    if (h->aused[set]) {
-        for (int i = 0; i < kCopyStreams; ++i) {
-            if ((e = cudaStreamWaitEvent(st, h->afree[set][i], 0)) != cudaSuccess)
-                return cuda_fail(e, "cudaStreamWaitEvent");
-        }
-    }
-    if ((rc = spread_copies(h->up, dg, host_grads, h->world, bytes, cudaMemcpyHostToDevice, st, true))) return rc;
-    if ((rc = zero1_step(h, dg, dp, stream))) return rc;
-    if ((rc = spread_copies(h->down, host_params, dp, h->world, bytes, cudaMemcpyDeviceToHost, st, false)))
-        return rc;
-    for (int i = 0; i < kCopyStreams; ++i)
-        if ((e = cudaEventRecord(h->afree[set][i], h->down.s[i])) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-    h->aused[set] = true;
-    h->aset = 1 - set;
-    return ZERO1_OK;
+    return host_step(h, host_grads, host_params, static_cast<cudaStream_t>(stream), false);
 }
 
 int zero1_host_sync(zero1_handle h)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    HostPath &P = h->host;
+    if (!P.ready) return ZERO1_OK;
     DeviceGuard g(h->device);
-    for (CopyLanes *l : {&h->up, &h->down, &h->copy}) {
-        if (!l->ready) continue;
-        for (int i = 0; i < kCopyStreams; ++i) {
-            cudaError_t e = cudaStreamSynchronize(l->s[i]);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-        }
+    for (cudaStream_t x : {P.up[0], P.up[1], P.rs, P.upd, P.down[0], P.down[1]}) {
+        cudaError_t e = cudaStreamSynchronize(x);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     }
+    P.pending = false;
     return ZERO1_OK;
 }
 
@@ -601,6 +734,8 @@ int zero1_set_state_range(zero1_handle h, uint64_t offset, uint64_t count, const
     if (count == 0) return ZERO1_OK;
     DeviceGuard g(h->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = join_host(h, st);
+    if (rc) return rc;
     const uint64_t bytes = count * sizeof(float);
     cudaError_t e;
     if ((e = cudaMemcpyAsync(h->master + offset, master, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
@@ -623,6 +758,8 @@ int zero1_get_state_range(zero1_handle h, uint64_t offset, uint64_t count, float
     if (count == 0) return ZERO1_OK;
     DeviceGuard g(h->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = join_host(h, st);
+    if (rc) return rc;
     const uint64_t bytes = count * sizeof(float);
     cudaError_t e;
     if (master && (e = cudaMemcpyAsync(master, h->master + offset, bytes, cudaMemcpyDefault, st)) != cudaSuccess)
@@ -698,6 +835,8 @@ int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *st
     DeviceGuard g(h->device);
     zero1::DevStatus st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = join_host(h, s);
+    if (rc) return rc;
     cudaError_t e = cudaMemcpyAsync(&st, h->status, sizeof st, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
@@ -797,6 +936,7 @@ int zero1_bucket_begin(zero1_handle h)
 {
     if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
     if (h->bucket_open) return fail(ZERO1_EINVAL, "a bucketed step is already open");
+    if (h->host.pending) return fail(ZERO1_EINVAL, "host-buffer steps are in flight; call zero1_host_sync first");
     DeviceGuard g(h->device);
     cudaError_t e;
     if (!h->bucket_sums &&
@@ -824,6 +964,7 @@ namespace {
 int check_bucket(zero1_ctx *h, uint64_t offset, uint64_t count, const void *const *ptrs, int mode)
 {
     if (!h->bucket_open) return fail(ZERO1_EINVAL, "no bucketed step is open (call zero1_bucket_begin)");
+    if (h->host.pending) return fail(ZERO1_EINVAL, "host-buffer steps are in flight; call zero1_host_sync first");
     if (h->bucket_mode != 0 && h->bucket_mode != mode)
         return fail(ZERO1_EINVAL, "one bucketed step uses zero1_bucket_reduce or zero1_bucket_update, not both");
     if (count == 0 || offset > h->n || count > h->n - offset)
@@ -848,28 +989,8 @@ int check_bucket(zero1_ctx *h, uint64_t offset, uint64_t count, const void *cons
 // Reduce-scatter + norm partial of one bucket (K1 in bucket mode).
 int launch_bucket_rs(zero1_ctx *h, uint64_t offset, uint64_t count, const void *const *grad_ptrs, cudaStream_t st)
 {
-    zero1::StepLaunch s;
-    s.grads = grad_ptrs;
-    s.params = nullptr;
-    s.world = h->world;
-    s.n = count;
-    s.master = h->master;
-    s.m = h->m;
-    s.v = h->v;
-    s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
-    s.partials = h->partials;
-    s.status = h->status;
-    s.sc = launch_scalars(h, h->t + 1);
-    s.max_norm = h->hp.max_norm;
-    s.clip_eps = h->opts.clip_eps;
-    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
-    if (h->opts.bucket_ctas > 0 && s.grid_rs > h->opts.bucket_ctas) s.grid_rs = h->opts.bucket_ctas;
-    s.phase = 1;
-    s.bucket_sums = h->bucket_sums;
-    s.bucket_index = (int)h->buckets.size();
-    cudaError_t e = zero1::launch_step(s, st, nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-    return ZERO1_OK;
+    return launch_rs_piece(h, offset, count, grad_ptrs, h->ghat ? h->ghat : h->ghat_bucket, h->bucket_sums,
+                           (int)h->buckets.size(), h->opts.bucket_ctas, st);
 }
 
 }  // namespace
@@ -902,29 +1023,9 @@ int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const v
     if ((rc = launch_bucket_rs(h, offset, count, grad_ptrs, st))) return rc;
     // The update of the bucket's parameters right away (c = 1 without
     // clipping); CTA 0 also records the norm of the buckets so far.
-    zero1::StepLaunch s;
-    s.grads = nullptr;
-    s.params = param_ptrs;
-    s.world = h->world;
-    s.n = count;
-    s.master = h->master + offset;
-    s.m = h->m + offset * h->msz;
-    s.v = h->v + offset * h->msz;
-    s.ghat = (h->ghat ? h->ghat : h->ghat_bucket) + offset;
-    s.partials = h->partials;
-    s.status = h->status;
-    s.sc = launch_scalars(h, h->t + 1);
-    s.max_norm = h->hp.max_norm;
-    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
-    if (h->opts.bucket_ctas > 0 && s.grid_update > h->opts.bucket_ctas) s.grid_update = h->opts.bucket_ctas;
-    s.moments_bf16 = h->opts.moments_bf16 != 0;
-    s.decay_first = h->opts.decay_before_update != 0;
-    s.clip_eps = h->opts.clip_eps;
-    s.phase = 2;
-    s.bucket_sums = h->bucket_sums;
-    s.nbuckets = (int)h->buckets.size() + 1;
-    cudaError_t e = zero1::launch_step(s, st, nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    if ((rc = launch_update_piece(h, offset, count, param_ptrs, h->ghat ? h->ghat : h->ghat_bucket, h->bucket_sums,
+                                  (int)h->buckets.size() + 1, false, true, h->opts.bucket_ctas, st)))
+        return rc;
     h->buckets.emplace_back(offset, count);
     h->bucket_mode = 2;
     return ZERO1_OK;

@@ -81,6 +81,7 @@ struct StepLaunch {
     // 8-parameter vectors per thread (see small_step_vpt)
     int small_vpt = 0;
     DevScalars dev{};       // capturable handles
+    bool advance_t = true;  // capturable: the update launch advances the device step counter
     bool stall_test = false; // failure test: the update kernel's waits run out (zero1_options)
 };
 

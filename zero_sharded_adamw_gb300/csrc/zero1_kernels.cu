@@ -82,6 +82,12 @@ struct UpdConfig {
 constexpr UpdConfig kUpdSpillF32{ZERO1_UPD_SPILL_F32_STAGES, ZERO1_UPD_SPILL_F32_WARPS};      // fp32 scratch, fp32 moments
 constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_STAGES, ZERO1_UPD_SPILL_BF16_WARPS};   // fp32 scratch, bf16 moments
 constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS};              // gradients re-read (W <= 2)
+// Update kernel tile order: 0 = grid-strided (CTA b takes tiles
+// ntiles-1-b, ntiles-1-b-G, ...), 1 = contiguous runs (CTA b takes the
+// tiles [b*ntiles/G, (b+1)*ntiles/G), from the top down).
+#ifndef ZERO1_UPD_RUNS
+#define ZERO1_UPD_RUNS 0
+#endif
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
@@ -126,6 +132,7 @@ struct UpdParams {
     int nbuckets;
     double max_norm, clip_eps;
     DevScalars dev;              // capturable: scalars formed from the device step counter
+    int advance_t;               // capturable: this launch ends the step (advances the counter)
     int stall_test;              // failure test: the producer issues nothing, so every wait runs out
 };
 
@@ -539,7 +546,17 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
     const int64_t ntiles = (int64_t)((nel + kUpdTile - 1) / kUpdTile);
+    // This CTA's tiles, k = 0 .. ncta-1, highest first.
+#if ZERO1_UPD_RUNS
+    const int64_t run_hi = (int64_t)(((uint64_t)blockIdx.x + 1) * (uint64_t)ntiles / gridDim.x);
+    const int64_t run_lo = (int64_t)((uint64_t)blockIdx.x * (uint64_t)ntiles / gridDim.x);
+    const uint32_t ncta = (uint32_t)(run_hi - run_lo);
+    auto tile_at = [&](uint32_t k) -> int64_t { return run_hi - 1 - (int64_t)k; };
+#else
     const int64_t first = ntiles - 1 - (int64_t)blockIdx.x;
+    const uint32_t ncta = first >= 0 ? (uint32_t)(first / gridDim.x + 1) : 0u;
+    auto tile_at = [&](uint32_t k) -> int64_t { return first - (int64_t)k * gridDim.x; };
+#endif
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
 
@@ -570,12 +587,14 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
         }
         if (p.dev.bc) {
             // Capturable: this step is t + 1.  The CTA that counts in last
-            // (every CTA has read t by then) advances the counter.
+            // (every CTA has read t by then) advances the counter, unless
+            // later launches of the same step (a step cut into pieces)
+            // still have to read it.
             const unsigned long long t = p.status->t + 1;
             sm.sc = form_scalars(p.sc, p.dev, t);
             __threadfence();
             if (atomicAdd(&p.status->ticket2, 1u) == gridDim.x - 1) {
-                p.status->t = t;
+                if (p.advance_t) p.status->t = t;
                 p.status->ticket2 = 0u;
             }
         } else {
@@ -591,7 +610,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     if (warp == kUpdConsumerWarps) {                              // producer
         if (lane == 0 && !p.stall_test) {
             uint32_t k = 0;
-            for (int64_t j = first; j >= 0 && !*abort; j -= gridDim.x, ++k) {
+            for (; k < ncta && !*abort; ++k) {
+                const int64_t j = tile_at(k);
                 const int s = k % kUpdStages;
                 if (k >= kUpdStages && !mbar_wait(&sm.empty[s], ((k / kUpdStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
                 const uint64_t base = (uint64_t)j * kUpdTile;
@@ -620,7 +640,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 
     if (warp == kUpdConsumerWarps + 1) {                          // stores
         uint32_t k = 0;
-        for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
+        for (; k < ncta; ++k) {
+            const int64_t j = tile_at(k);
             const int s = k % kUpdStages;
             const bool got = mbar_wait(&sm.done[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
@@ -658,8 +679,8 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     // line: a bucket that begins mid-line (a multiple of 8 parameters, not
     // of 32) must not drop its neighbour's unread values.
     const bool discard = !REREAD && (reinterpret_cast<uintptr_t>(p.ghat) & 127u) == 0;
-    uint32_t k = 0;
-    for (int64_t j = first; j >= 0; j -= gridDim.x, ++k) {
+    for (uint32_t k = 0; k < ncta; ++k) {
+        const int64_t j = tile_at(k);
         const int s = k % kUpdStages;
         const bool got = mbar_wait(&sm.full[s], (k / kUpdStages) & 1u, abort, &p.status->errors);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
@@ -1038,6 +1059,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     up.max_norm = s.max_norm;
     up.clip_eps = s.clip_eps;
     up.dev = s.dev;
+    up.advance_t = s.advance_t ? 1 : 0;
     up.stall_test = s.stall_test ? 1 : 0;
 
     const bool spill = s.ghat != nullptr;
