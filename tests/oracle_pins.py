@@ -578,6 +578,68 @@ def pin_bf16_moments_vs_torch_inplace_ops():
         assert np.mean(st.master.view(np.uint32) == p.numpy().view(np.uint32)) >= 0.999
 
 
+def pin_fp32_update_vs_torch_inplace_ops():
+    """The fp32 update against the page's own in-place ops run by torch on
+    fp32 tensors: m.mul_(b1).add_(g, alpha=1-b1),
+    v.mul_(b2).addcmul_(g, g, value=1-b2),
+    p.addcdiv_(m, v.sqrt().add_(eps), value=-step_size), p.mul_(1-lr*wd),
+    step by step from the oracle's own state (W = 1, no clipping, so the
+    step sees g exactly).
+    At the first step m = v = 0, so every op is a product with one rounding
+    whatever torch fuses: there the oracle's m and v equal torch's in every
+    element, which fixes the association of the second-moment term,
+    ((1-b2)*g)*g, against (1-b2)*(g*g) (the two disagree in about 30% of
+    bf16 gradients).  Afterwards torch's kernels fuse the multiply-add
+    (one rounding of a*x + y) where the reading rounds the product first,
+    so the two agree in most elements (m >= 60%, v >= 80%, master >= 90%)
+    and every moment difference is within what one skipped product rounding
+    and the final rounding allow: 2^-24 |product| + 2^-23 |result|.  For the
+    master, torch's addcdiv scales m before dividing by d, while the reading
+    takes the text's step direction m / (sqrt(v) + eps) and scales that, so
+    the bound is two ulps of the scaled step, the two final roundings
+    (update, then decay) and what the step's own m and v differences carry
+    into step_size * m / d."""
+    rng = np.random.default_rng(43)
+    n = 20_000
+    hp = o.HP(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.0)
+    st = o.State((rng.standard_normal(n) * 0.02).astype(np.float32))
+    same = lambda a, b: np.mean(a.view(np.uint32) == b.view(np.uint32))
+    for t in range(1, 7):
+        g = rand_bf16(rng, n, 1e-2)
+        gt = torch.from_numpy(torch_widen(g).astype(np.float32))
+        m, v, p = (torch.from_numpy(x.copy()) for x in (st.m, st.v, st.master))
+        sc = o.step_scalars(hp, 1, t)
+        m.mul_(hp.beta1).add_(gt, alpha=1 - hp.beta1)
+        v.mul_(hp.beta2).addcmul_(gt, gt, value=1 - hp.beta2)
+        p.addcdiv_(m, v.sqrt().add_(hp.eps), value=-float(sc["step_size"]))
+        p.mul_(float(sc["decay"]))
+        assert st.t == t - 1
+        o.step(st, [g], hp)
+        tm, tv, tp = m.numpy(), v.numpy(), p.numpy()
+        if t == 1:
+            assert same(st.m, tm) == 1.0 and same(st.v, tv) == 1.0
+        assert same(st.m, tm) >= 0.6 and same(st.v, tv) >= 0.8 and same(st.master, tp) >= 0.9
+        g64 = torch_widen(g).astype(np.float64)
+        m64, v64 = tm.astype(np.float64), tv.astype(np.float64)
+        d64 = np.sqrt(v64) + hp.eps
+        step = float(sc["step_size"])
+        # The master: torch's addcdiv forms (value * m) / d, where the reading
+        # follows the text's step direction m / d and then scales it; each
+        # side rounds that scaled step twice (within one ulp of it), so they
+        # differ by up to two; the step direction also carries the moments'
+        # differences, and two rounded ops follow (the update, the decay).
+        dm = np.abs(st.m.astype(np.float64) - m64)
+        dd = np.abs(st.v.astype(np.float64) - v64) / (2.0 * np.sqrt(np.maximum(v64, 1e-300)))
+        carried = step * (dm / d64 + np.abs(m64) * dd / (d64 * d64))
+        for ours, theirs, prod, k_prod, k_res, extra in (
+                (st.m, tm, (1 - hp.beta1) * np.abs(g64), 0.5, 1, 0.0),
+                (st.v, tv, (1 - hp.beta2) * g64 * g64, 0.5, 1, 0.0),
+                (st.master, tp, step * np.abs(m64) / d64, 2, 2, carried)):
+            a, b = ours.astype(np.float64), theirs.astype(np.float64)
+            bound = 1.001 * (2.0 ** -23 * (k_prod * prod + k_res * np.maximum(np.abs(a), np.abs(b))) + extra)
+            assert (np.abs(a - b) <= bound).all(), t
+
+
 def pin_ddp_linearity():
     """The printed DDP check (float64): the mean of the 4 shard gradients is
     the full-batch gradient.  The oracle's reduce-scatter mean of the bf16

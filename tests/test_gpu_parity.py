@@ -131,16 +131,20 @@ def test_one_launch_selection():
         z.Zero1(16, 2, None, z.Options(small_step=2))
 
 
-def test_multi_tile_ragged_clip_on_and_off():
-    base = WL.WORKLOADS["ragged_1p3b"].with_n(1_000_003)
-    run_parity(base, 3)
+@pytest.mark.parametrize("name,n", [("gpt2_small", 2_000_003), ("ragged_1p3b", 1_000_003),
+                                    ("state_7b", 1_000_003), ("stress_w64", 200_001)])
+def test_recipe_for_its_configured_steps(name, n):
+    """Each large recipe (its W, gradient distribution, outliers, rank mean
+    offsets and clip threshold) at a size the oracle runs in seconds, for the
+    number of steps the recipe is configured with (20, 10, 5 and 5): every
+    step bit-exact with the GPU's clip coefficient injected, and the GPU
+    state within 1e-6 of a free-running oracle after each step."""
+    w = WL.WORKLOADS[name].with_n(n)
+    run_parity(w, w.steps)
+
+
+def test_multi_tile_ragged_without_clipping():
     run_parity(WL.Workload("noclip", 1_000_003, 8, 1e-3, 3, max_norm=0.0), 3)
-
-
-def test_stress_shape_small():
-    """The W = 64 recipe (rank mean offsets, clip 0.5) at a size the oracle
-    runs in seconds."""
-    run_parity(WL.WORKLOADS["stress_w64"].with_n(200_001), 3)
 
 
 def test_lr_schedule():

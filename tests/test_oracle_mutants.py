@@ -38,6 +38,7 @@ MUTANTS = {
                             "float s = zref_bf16_to_f32(grads[world - 1][i]);\n        for (int q = world - 2; q >= 0; --q)\n            s = s + zref_bf16_to_f32(grads[q][i]);"),
     "m_without_one_minus_beta1": ("mi = mi + s->one_minus_beta1 * g;", "mi = mi + g;"),
     "v_linear_in_g": ("vi = vi + og * g;", "vi = vi + og;"),
+    "v_term_reassociated": ("vi = vi + og * g;", "vi = vi + s->one_minus_beta2 * (g * g); (void)og;"),
     "m_uses_beta2": ("float mi = s->beta1 * m[i];", "float mi = s->beta2 * m[i];"),
     "update_sign_flipped": ("float p = master[i] - s->step_size * u;", "float p = master[i] + s->step_size * u;"),
     "shard_drops_last_element": ("uint64_t a = (uint64_t)r * s, b = a + s;", "uint64_t a = (uint64_t)r * s, b = a + s - 1;"),
@@ -70,8 +71,8 @@ def source():
         return f.read()
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name, source, tmp_path):
+def _catchers(name, source, tmp_path) -> list[str]:
+    """The pins that fail on the oracle with mutant `name` planted."""
     old, new = MUTANTS[name]
     assert source.count(old) >= 1, f"mutation site for {name} not found"
     src = tmp_path / "mutant.c"
@@ -88,4 +89,17 @@ def test_mutant_is_caught(name, source, tmp_path):
                 caught.append(pin.__name__)
     finally:
         o.use(prev)
-    assert caught, f"no pin caught the planted mistake {name}"
+    return caught
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    assert _catchers(name, source, tmp_path), f"no pin caught the planted mistake {name}"
+
+
+def test_second_moment_association_needs_the_inplace_ops_pin(source, tmp_path):
+    """(1-b2)*(g*g) in place of ((1-b2)*g)*g stays within the 1e-6 parity
+    tolerance and passes the closed forms and the float64 torch.optim.AdamW
+    comparison; the page's in-place ops run by torch on fp32 tensors are
+    what tell the two associations apart."""
+    assert _catchers("v_term_reassociated", source, tmp_path) == ["pin_fp32_update_vs_torch_inplace_ops"]
