@@ -29,10 +29,13 @@
 #include "zero1.h"
 #include "zero1_internal.h"
 
-// Slots in each of the host path's two device rings (uploads, downloads).
-constexpr int kHostSlots = 4;
+// Slots in each of the host path's two device rings (uploads, downloads),
+// and the copy streams each direction's chunks are dealt over (one copy
+// engine each, so that several run at once).
+constexpr int kHostSlots = 8;
+constexpr int kHostCopyStreams = 4;
 // Device bytes of one slot by default: the W ranks' bf16 slices of one chunk.
-constexpr uint64_t kHostSlotBytes = 128ull << 20;
+constexpr uint64_t kHostSlotBytes = 64ull << 20;
 constexpr uint64_t kHostChunkAlign = 2048;   // chunks start on whole update tiles
 
 // The host-buffer steps (zero1_step_host, zero1_step_host_async): gradients
@@ -54,7 +57,7 @@ struct HostPath {
     uint64_t rank_stride = 0;      // bytes between ranks' slices in a slot (256-byte rounded)
     void *staging = nullptr;       // kHostSlots upload slots, then kHostSlots download slots
     double *sums = nullptr;        // 2 parity sets x nchunks x (sum, plain sum)
-    cudaStream_t rs = nullptr, upd = nullptr, up[2] = {}, down[2] = {};
+    cudaStream_t rs = nullptr, upd = nullptr, up[kHostCopyStreams] = {}, down[kHostCopyStreams] = {};
     cudaEvent_t fork = nullptr, norm_done = nullptr, last = nullptr;
     cudaEvent_t up_ready[kHostSlots] = {}, up_free[kHostSlots] = {};
     cudaEvent_t down_ready[kHostSlots] = {}, down_free[kHostSlots] = {};
@@ -234,8 +237,11 @@ int join_host(zero1_ctx *h, cudaStream_t st)
 
 void release_host_path(HostPath &P)
 {
-    for (cudaStream_t x : {P.rs, P.upd, P.up[0], P.up[1], P.down[0], P.down[1]})
+    for (cudaStream_t x : {P.rs, P.upd})
         if (x) cudaStreamDestroy(x);
+    for (int i = 0; i < kHostCopyStreams; ++i)
+        for (cudaStream_t x : {P.up[i], P.down[i]})
+            if (x) cudaStreamDestroy(x);
     for (cudaEvent_t x : {P.fork, P.norm_done, P.last})
         if (x) cudaEventDestroy(x);
     for (int i = 0; i < kHostSlots; ++i)
@@ -365,7 +371,7 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
     h->msz = o.moments_bf16 ? 2 : sizeof(float);
     zero1_shard_plan(n, world, &h->shard, &h->padded);
     h->reread = world <= 2;
-    zero1::plan_grids(world, n, h->reread, h->num_sms, &h->grid_rs, &h->grid_update);
+    zero1::plan_grids(n, h->reread, h->num_sms, &h->grid_rs, &h->grid_update);
 
     // One allocation: master | m | v | ghat (W >= 3) | partials | status,
     // every section 256-byte aligned.
@@ -499,7 +505,7 @@ int launch_rs_piece(zero1_ctx *h, uint64_t offset, uint64_t count, const void *c
     s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
     s.clip_eps = h->opts.clip_eps;
-    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    zero1::plan_grids(count, false, h->num_sms, &s.grid_rs, &s.grid_update);
     if (max_ctas > 0 && s.grid_rs > max_ctas) s.grid_rs = max_ctas;
     s.phase = 1;
     s.bucket_sums = sums;
@@ -529,7 +535,7 @@ int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *con
     s.status = h->status;
     s.sc = launch_scalars(h, h->t + 1);
     s.max_norm = h->hp.max_norm;
-    zero1::plan_grids(h->world, count, false, h->num_sms, &s.grid_rs, &s.grid_update);
+    zero1::plan_grids(count, false, h->num_sms, &s.grid_rs, &s.grid_update);
     if (max_ctas > 0 && s.grid_update > max_ctas) s.grid_update = max_ctas;
     s.moments_bf16 = h->opts.moments_bf16 != 0;
     s.decay_first = h->opts.decay_before_update != 0;
@@ -583,7 +589,12 @@ int host_path_ready(zero1_ctx *h)
         Q.sums = nullptr;
         return undo(e, "cudaMalloc of the host-path norm partials");
     }
-    for (cudaStream_t *x : {&Q.rs, &Q.upd, &Q.up[0], &Q.up[1], &Q.down[0], &Q.down[1]})
+    std::vector<cudaStream_t *> sts = {&Q.rs, &Q.upd};
+    for (int i = 0; i < kHostCopyStreams; ++i) {
+        sts.push_back(&Q.up[i]);
+        sts.push_back(&Q.down[i]);
+    }
+    for (cudaStream_t *x : sts)
         if ((e = cudaStreamCreateWithFlags(x, cudaStreamNonBlocking)) != cudaSuccess) return undo(e, "cudaStreamCreate");
     std::vector<cudaEvent_t *> evs = {&Q.fork, &Q.norm_done, &Q.last};
     for (int i = 0; i < kHostSlots; ++i)
@@ -627,7 +638,7 @@ int host_step(zero1_ctx *h, const void *const *host_grads, void *const *host_par
     for (int i = 0; i < M; ++i) {                    // uploads and reduces
         const uint64_t lo = (uint64_t)i * P.chunk, cnt = std::min<uint64_t>(P.chunk, h->n - lo);
         const int sl = (int)(P.up_count % kHostSlots);
-        cudaStream_t u = P.up[P.up_count % 2];
+        cudaStream_t u = P.up[P.up_count % kHostCopyStreams];
         char *base = ring + (uint64_t)sl * slot_bytes;
         if (P.up_used[sl]) HOST_CHECK(cudaStreamWaitEvent(u, P.up_free[sl], 0), "cudaStreamWaitEvent");
         for (int r = 0; r < W; ++r) {
@@ -651,7 +662,7 @@ int host_step(zero1_ctx *h, const void *const *host_grads, void *const *host_par
     for (int i = 0; i < M; ++i) {                    // updates and downloads
         const uint64_t lo = (uint64_t)i * P.chunk, cnt = std::min<uint64_t>(P.chunk, h->n - lo);
         const int sl = (int)(P.down_count % kHostSlots);
-        cudaStream_t d = P.down[P.down_count % 2];
+        cudaStream_t d = P.down[P.down_count % kHostCopyStreams];
         char *base = ring + (uint64_t)(kHostSlots + sl) * slot_bytes;
         if (P.down_used[sl]) HOST_CHECK(cudaStreamWaitEvent(P.upd, P.down_free[sl], 0), "cudaStreamWaitEvent");
         for (int r = 0; r < W; ++r) pslot[r] = base + (uint64_t)r * P.rank_stride;
@@ -675,8 +686,8 @@ int host_step(zero1_ctx *h, const void *const *host_grads, void *const *host_par
     h->t += 1;
     if (blocking) {
         HOST_CHECK(cudaStreamWaitEvent(st, P.last, 0), "cudaStreamWaitEvent");
-        for (cudaStream_t x : {P.upd, P.down[0], P.down[1]})
-            HOST_CHECK(cudaStreamSynchronize(x), "cudaStreamSynchronize");
+        HOST_CHECK(cudaStreamSynchronize(P.upd), "cudaStreamSynchronize");
+        for (cudaStream_t x : P.down) HOST_CHECK(cudaStreamSynchronize(x), "cudaStreamSynchronize");
         P.pending = false;
     }
     return ZERO1_OK;
@@ -717,7 +728,11 @@ int zero1_host_sync(zero1_handle h)
     HostPath &P = h->host;
     if (!P.ready) return ZERO1_OK;
     DeviceGuard g(h->device);
-    for (cudaStream_t x : {P.up[0], P.up[1], P.rs, P.upd, P.down[0], P.down[1]}) {
+    std::vector<cudaStream_t> all(P.up, P.up + kHostCopyStreams);
+    all.push_back(P.rs);
+    all.push_back(P.upd);
+    all.insert(all.end(), P.down, P.down + kHostCopyStreams);
+    for (cudaStream_t x : all) {
         cudaError_t e = cudaStreamSynchronize(x);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     }
@@ -1060,30 +1075,9 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
         return ZERO1_OK;
     }
     DeviceGuard g(h->device);
-    zero1::StepLaunch s;
-    s.grads = nullptr;
-    s.params = param_ptrs;
-    s.world = h->world;
-    s.n = h->n;
-    s.master = h->master;
-    s.m = h->m;
-    s.v = h->v;
-    s.ghat = h->ghat ? h->ghat : h->ghat_bucket;
-    s.partials = h->partials;
-    s.status = h->status;
-    s.sc = launch_scalars(h, h->t + 1);
-    s.max_norm = h->hp.max_norm;
-    s.grid_rs = h->grid_rs;
-    s.grid_update = h->grid_update;
-    s.moments_bf16 = h->opts.moments_bf16 != 0;
-    s.decay_first = h->opts.decay_before_update != 0;
-    s.clip_eps = h->opts.clip_eps;
-    s.phase = 2;
-    s.dev = dev_scalars(h);
-    s.bucket_sums = h->bucket_sums;
-    s.nbuckets = (int)h->buckets.size();
-    cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    int rc = launch_update_piece(h, 0, h->n, param_ptrs, h->ghat ? h->ghat : h->ghat_bucket, h->bucket_sums,
+                                 (int)h->buckets.size(), true, true, 0, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
     h->bucket_open = false;
     h->t += 1;
     return ZERO1_OK;

@@ -122,7 +122,7 @@ cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
 cudaError_t set_func_attribute_once(const void *kernel, cudaFuncAttribute attr, int value);
 
 // Grid sizes: one wave of resident CTAs on this device, capped by the work.
-void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);
+void plan_grids(uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update);
 
 // Set the message zero1_last_error() returns on this thread.
 void set_error_message(const char *msg);

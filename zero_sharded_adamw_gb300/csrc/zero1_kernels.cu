@@ -57,42 +57,51 @@ constexpr int kTile = 2048;                      // parameters per tile
 #define ZERO1_PDL 0
 #endif
 constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel (3 and 2 measured slower)
-// The update kernel's ring depth and consumer warps, per path (measured on
-// GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment workloads): with an
-// fp32 scratch and fp32 moments the kernel is write-heavy (16 B read, 24 + 2W
-// written per parameter) and runs fastest with 3 stages in flight and 16
-// consumer warps; the gradient re-read (W <= 2) and bf16-moment paths run
-// fastest with 4 stages and 8 warps.
+// The update kernel's tile, ring depth, consumer warps and tile order, per
+// path (measured on GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment
+// workloads):
+//  - fp32 scratch, fp32 moments: write-heavy (16 B read, 24 + 2W written per
+//    parameter); fastest with 2048-parameter tiles, 3 stages in flight and 16
+//    consumer warps, tiles grid-strided;
+//  - fp32 scratch, bf16 moments: 2048-parameter tiles, 4 stages, 8 warps;
+//  - gradient re-read (W <= 2): 4096-parameter tiles, 3 stages, 8 warps, and
+//    each CTA walking one contiguous run of tiles (1.5% faster than 2048 x 4
+//    grid-strided at 2B parameters; the other paths lose 1-2% with runs).
+// Tile order: grid-strided = CTA b takes tiles ntiles-1-b, ntiles-1-b-G, ...;
+// runs = CTA b takes [b*ntiles/G, (b+1)*ntiles/G), from the top down.
 struct UpdConfig {
-    int stages, warps;
+    int tile, stages, warps;
+    bool runs;
 };
-// (-D overrides for tuning: ZERO1_UPD_<PATH>_STAGES / _WARPS.)
+// (-D overrides for tuning: ZERO1_UPD_<PATH>_TILE / _STAGES / _WARPS / _RUNS.)
 #ifndef ZERO1_UPD_SPILL_F32_STAGES
+#define ZERO1_UPD_SPILL_F32_TILE 2048
 #define ZERO1_UPD_SPILL_F32_STAGES 3
 #define ZERO1_UPD_SPILL_F32_WARPS 16
+#define ZERO1_UPD_SPILL_F32_RUNS false
 #endif
 #ifndef ZERO1_UPD_SPILL_BF16_STAGES
+#define ZERO1_UPD_SPILL_BF16_TILE 2048
 #define ZERO1_UPD_SPILL_BF16_STAGES 4
 #define ZERO1_UPD_SPILL_BF16_WARPS 8
+#define ZERO1_UPD_SPILL_BF16_RUNS false
 #endif
 #ifndef ZERO1_UPD_REREAD_STAGES
-#define ZERO1_UPD_REREAD_STAGES 4
+#define ZERO1_UPD_REREAD_TILE 4096
+#define ZERO1_UPD_REREAD_STAGES 3
 #define ZERO1_UPD_REREAD_WARPS 8
+#define ZERO1_UPD_REREAD_RUNS true
 #endif
-constexpr UpdConfig kUpdSpillF32{ZERO1_UPD_SPILL_F32_STAGES, ZERO1_UPD_SPILL_F32_WARPS};      // fp32 scratch, fp32 moments
-constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_STAGES, ZERO1_UPD_SPILL_BF16_WARPS};   // fp32 scratch, bf16 moments
-constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS};              // gradients re-read (W <= 2)
-// Update kernel tile order: 0 = grid-strided (CTA b takes tiles
-// ntiles-1-b, ntiles-1-b-G, ...), 1 = contiguous runs (CTA b takes the
-// tiles [b*ntiles/G, (b+1)*ntiles/G), from the top down).
-#ifndef ZERO1_UPD_RUNS
-#define ZERO1_UPD_RUNS 0
-#endif
+constexpr UpdConfig kUpdSpillF32{ZERO1_UPD_SPILL_F32_TILE, ZERO1_UPD_SPILL_F32_STAGES, ZERO1_UPD_SPILL_F32_WARPS,
+                                 ZERO1_UPD_SPILL_F32_RUNS};      // fp32 scratch, fp32 moments
+constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_TILE, ZERO1_UPD_SPILL_BF16_STAGES, ZERO1_UPD_SPILL_BF16_WARPS,
+                                  ZERO1_UPD_SPILL_BF16_RUNS};   // fp32 scratch, bf16 moments
+constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_TILE, ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS,
+                               ZERO1_UPD_REREAD_RUNS};          // gradients re-read (W <= 2)
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kRsThreads = kConsumers + 32;      // + producer warp
-constexpr int kUpdTile = kTile;                  // parameters per update-kernel tile
 static_assert(kConsumers * kVec == kTile, "one 8-parameter vector per consumer thread");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -455,11 +464,11 @@ __device__ __forceinline__ void adamw1(float gh, float c, const StepScalars &s, 
     v = vi;
 }
 
-template <int STAGES>
+template <int TILE, int STAGES>
 struct UpdSmem {
-    float in[STAGES][4][kUpdTile];   // 32 KB per stage: ghat (or the W <= 2 bf16 grads), master, m, v
+    float in[STAGES][4][TILE];     // 16*TILE bytes per stage: ghat (or the W <= 2 bf16 grads), master, m, v
                                    // (m, v use half their slot when stored in bf16)
-    uint16_t b16[STAGES][kUpdTile];  // 4 KB per stage: the tile's bf16 parameters
+    uint16_t b16[STAGES][TILE];    // 2*TILE bytes per stage: the tile's bf16 parameters
     uint64_t full[STAGES], done[STAGES], empty[STAGES];
     int abort;
     float clip;
@@ -468,8 +477,8 @@ struct UpdSmem {
 
 // Four consecutive parameters at offset o of stage s: AdamW in place on the
 // staged master, m, v and the bf16 values into the replica tile.
-template <bool REREAD, bool MV16, int STAGES>
-__device__ __forceinline__ void update4(UpdSmem<STAGES> &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc,
+template <bool REREAD, bool MV16, int TILE, int STAGES>
+__device__ __forceinline__ void update4(UpdSmem<TILE, STAGES> &sm, int s, uint32_t o, int nw, float c, const StepScalars &sc,
                                         bool decay_first)
 {
     float gh[4];
@@ -481,7 +490,7 @@ __device__ __forceinline__ void update4(UpdSmem<STAGES> &sm, int s, uint32_t o, 
         gh[2] = __uint_as_float(raw.y << 16);
         gh[3] = __uint_as_float(raw.y & 0xFFFF0000u);
         for (int r = 1; r < nw; ++r) {
-            raw = *reinterpret_cast<const uint2 *>(g + r * kUpdTile + o);
+            raw = *reinterpret_cast<const uint2 *>(g + r * TILE + o);
             gh[0] = __fadd_rn(gh[0], __uint_as_float(raw.x << 16));
             gh[1] = __fadd_rn(gh[1], __uint_as_float(raw.x & 0xFFFF0000u));
             gh[2] = __fadd_rn(gh[2], __uint_as_float(raw.y << 16));
@@ -530,11 +539,12 @@ __device__ __forceinline__ void update4(UpdSmem<STAGES> &sm, int s, uint32_t o, 
 // from the highest down (the reduce-scatter kernel wrote those last, so
 // they are the likeliest to still be in L2).  master, m, v are updated in
 // place in the stage and written back from there.
-template <int W, int CAP, bool REREAD, bool MV16, int STAGES, int CWARPS>
+template <int W, int CAP, bool REREAD, bool MV16, int TILE, int STAGES, int CWARPS, bool RUNS>
 __global__ void __launch_bounds__(CWARPS * 32 + 64, 1)
 zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 {
     constexpr uint32_t kMomBytes = MV16 ? 2u : 4u;   // bytes per stored moment
+    constexpr int kUpdTile = TILE;
     constexpr int kUpdStages = STAGES;
     constexpr int kUpdConsumerWarps = CWARPS;
     constexpr int kUpdConsumers = CWARPS * 32;
@@ -542,21 +552,20 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
     static_assert(kUpdQuads >= 1 && kUpdQuads * 4 * kUpdConsumers == kUpdTile, "update consumers must tile kUpdTile");
     static_assert(kUpdTile / 32 <= kUpdConsumers, "one discarded scratch line per consumer thread");
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    UpdSmem<STAGES> &sm = *reinterpret_cast<UpdSmem<STAGES> *>(smem_raw);
+    UpdSmem<TILE, STAGES> &sm = *reinterpret_cast<UpdSmem<TILE, STAGES> *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
     const uint64_t nel = p.nvec * kVec;
     const int64_t ntiles = (int64_t)((nel + kUpdTile - 1) / kUpdTile);
-    // This CTA's tiles, k = 0 .. ncta-1, highest first.
-#if ZERO1_UPD_RUNS
-    const int64_t run_hi = (int64_t)(((uint64_t)blockIdx.x + 1) * (uint64_t)ntiles / gridDim.x);
+    // This CTA's tiles, k = 0 .. ncta-1, highest first: one contiguous run
+    // (RUNS), or every gridDim.x-th tile.
+    const int64_t run_hi = RUNS ? (int64_t)(((uint64_t)blockIdx.x + 1) * (uint64_t)ntiles / gridDim.x)
+                                : ntiles - 1 - (int64_t)blockIdx.x;
     const int64_t run_lo = (int64_t)((uint64_t)blockIdx.x * (uint64_t)ntiles / gridDim.x);
-    const uint32_t ncta = (uint32_t)(run_hi - run_lo);
-    auto tile_at = [&](uint32_t k) -> int64_t { return run_hi - 1 - (int64_t)k; };
-#else
-    const int64_t first = ntiles - 1 - (int64_t)blockIdx.x;
-    const uint32_t ncta = first >= 0 ? (uint32_t)(first / gridDim.x + 1) : 0u;
-    auto tile_at = [&](uint32_t k) -> int64_t { return first - (int64_t)k * gridDim.x; };
-#endif
+    const uint32_t ncta = RUNS ? (uint32_t)(run_hi - run_lo)
+                               : (run_hi >= 0 ? (uint32_t)(run_hi / gridDim.x + 1) : 0u);
+    auto tile_at = [&](uint32_t k) -> int64_t {
+        return RUNS ? run_hi - 1 - (int64_t)k : run_hi - (int64_t)k * gridDim.x;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
 
@@ -695,7 +704,7 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
 #pragma unroll
         for (int q = 0; q < kUpdQuads; ++q) {
             const uint32_t o = threadIdx.x * 4u + (uint32_t)q * 4u * kUpdConsumers;
-            if (o < cnt) update4<REREAD, MV16, STAGES>(sm, s, o, nw, c, sc, p.decay_first != 0);
+            if (o < cnt) update4<REREAD, MV16, TILE, STAGES>(sm, s, o, nw, c, sc, p.decay_first != 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -1065,16 +1074,17 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
     auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
-    constexpr int S1 = kUpdSpillF32.stages, C1 = kUpdSpillF32.warps;
-    constexpr int S2 = kUpdSpillBf16.stages, C2 = kUpdSpillBf16.warps;
-    constexpr int S0 = kUpdReread.stages, C0 = kUpdReread.warps;
+    constexpr UpdConfig U1 = kUpdSpillF32, U2 = kUpdSpillBf16, U0 = kUpdReread;
+    constexpr int C1 = U1.warps, C2 = U2.warps, C0 = U0.warps;
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
     const int path = spill ? (s.moments_bf16 ? 2 : 1) : 0;
-    auto k2 = path == 1   ? zero1_adamw_ag_kernel<W, CAP, false, false, S1, C1>
-              : path == 2 ? zero1_adamw_ag_kernel<W, CAP, false, true, S2, C2>
-                          : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true, S0, C0>
-                                            : zero1_adamw_ag_kernel<W, CAP, true, false, S0, C0>);
-    const size_t k2_smem = path == 1 ? sizeof(UpdSmem<S1>) : path == 2 ? sizeof(UpdSmem<S2>) : sizeof(UpdSmem<S0>);
+    auto k2 = path == 1   ? zero1_adamw_ag_kernel<W, CAP, false, false, U1.tile, U1.stages, C1, U1.runs>
+              : path == 2 ? zero1_adamw_ag_kernel<W, CAP, false, true, U2.tile, U2.stages, C2, U2.runs>
+                          : (s.moments_bf16 ? zero1_adamw_ag_kernel<W, CAP, true, true, U0.tile, U0.stages, C0, U0.runs>
+                                            : zero1_adamw_ag_kernel<W, CAP, true, false, U0.tile, U0.stages, C0, U0.runs>);
+    const size_t k2_smem = path == 1   ? sizeof(UpdSmem<U1.tile, U1.stages>)
+                           : path == 2 ? sizeof(UpdSmem<U2.tile, U2.stages>)
+                                       : sizeof(UpdSmem<U0.tile, U0.stages>);
     const int k2_threads = (path == 1 ? C1 : path == 2 ? C2 : C0) * 32 + 64;
     if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
     // A whole step without profiling events between its kernels launches
@@ -1123,18 +1133,19 @@ cudaError_t launch_step(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *e
     return launch_w<0, 512>(s, stream, ev);
 }
 
-void plan_grids(int world, uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update)
+void plan_grids(uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_update)
 {
-    (void)world;
-    (void)reread;
-    // Persistent kernels: one CTA per SM (each holds ~130-150 KB of shared
+    // Persistent kernels: one CTA per SM (each holds ~130-220 KB of shared
     // memory), never more CTAs than tiles, at least one (the n % 8 tail).
+    // The update kernel's tile depends on its path (re-read or scratch).
     const uint64_t ntiles = (n / kVec * kVec + kTile - 1) / kTile;
     uint64_t g = (uint64_t)num_sms;
     if (ntiles < g) g = ntiles;
     if (g < 1) g = 1;
     *grid_rs = (int)g;
-    const uint64_t ntiles_upd = (n / kVec * kVec + kUpdTile - 1) / kUpdTile;
+    const uint64_t upd_tile = (uint64_t)(reread ? kUpdReread.tile : kUpdSpillF32.tile);
+    static_assert(kUpdSpillF32.tile == kUpdSpillBf16.tile, "the scratch paths share one tile size");
+    const uint64_t ntiles_upd = (n / kVec * kVec + upd_tile - 1) / upd_tile;
     uint64_t gu = (uint64_t)num_sms;
     if (ntiles_upd < gu) gu = ntiles_upd;
     if (gu < 1) gu = 1;

@@ -192,7 +192,7 @@ extern "C" int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp
     s.sc = zero1::StepScalars{sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
     s.max_norm = hp->max_norm;
     s.small_vpt = zero1::small_step_vpt(n, world, 0);
-    zero1::plan_grids(world, n, reread, num_sms, &s.grid_rs, &s.grid_update);
+    zero1::plan_grids(n, reread, num_sms, &s.grid_rs, &s.grid_update);
     if ((size_t)s.grid_rs * 2 > kPartialDoubles)
         return nfail(ZERO1_EINVAL, "grid of %d CTAs exceeds the fixed partials scratch", s.grid_rs);
 
