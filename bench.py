@@ -518,12 +518,23 @@ def zero2_arm(args, w: WL.Workload):
     x = torch.randn(args.tokens, d_model, device=dev, dtype=torch.bfloat16)
     mats = {cnt: torch.randn(d_model, max(128, cnt // d_model // 128 * 128), device=dev, dtype=torch.bfloat16)
             for _, cnt in cuts}
-    opt = z.Zero1(w.n, w.world, hp, z.Options(bucket_ctas=args.bucket_ctas))
+    # --partition K: the device's SMs split into two green contexts, K (or
+    # the driver's rounding of it) for the bucket reduces and the rest for
+    # the backward, whose persistent GEMMs would otherwise hold every SM.
+    part = z.SmPartition(args.partition) if args.partition > 0 else None
+    bucket_ctas = part.sms_a if part else args.bucket_ctas
+    opt = z.Zero1(w.n, w.world, hp, z.Options(bucket_ctas=bucket_ctas))
     opt.set_state(WL.master(w, dev))
-    # Both streams are ordinary (non-default) streams: the legacy default
-    # stream would serialise against the other.
+    # Ordinary (non-default) streams: the legacy default stream would
+    # serialise against the others.  The optimizer's closing kernel runs on
+    # `main` with every SM; the backward runs on `bwd`.
     main = torch.cuda.Stream(dev)
-    comm = torch.cuda.Stream(dev, priority=-1)      # bucket reduces get SMs as soon as they free up
+    if part:
+        comm = torch.cuda.ExternalStream(part.stream_a, device=dev)
+        bwd = torch.cuda.ExternalStream(part.stream_b, device=dev)
+    else:
+        comm = torch.cuda.Stream(dev, priority=-1)  # bucket reduces get SMs as soon as they free up
+        bwd = main
 
     sleep_cycles = int(args.sleep_us * 1e-6 * 2.07e9)
 
@@ -536,12 +547,15 @@ def zero2_arm(args, w: WL.Workload):
 
     def run(mode):
         evs = []
-        for off, cnt in cuts:
-            backward_bucket(cnt)
-            if mode == "overlap":
-                ev = torch.cuda.Event()
-                ev.record(main)
-                evs.append((off, cnt, ev))
+        bwd.wait_stream(main)                   # this iteration's backward follows the last update
+        with torch.cuda.stream(bwd):
+            for off, cnt in cuts:
+                backward_bucket(cnt)
+                if mode == "overlap":
+                    ev = torch.cuda.Event()
+                    ev.record(bwd)
+                    evs.append((off, cnt, ev))
+        main.wait_stream(bwd)
         if mode == "seq":
             opt.step(grads, reps, main)
         elif mode == "overlap":
@@ -556,14 +570,6 @@ def zero2_arm(args, w: WL.Workload):
             main.wait_stream(comm)
             z.zero1_bucket_finish(opt.handle, None if args.bucket_update else reps, main)
 
-    # Blackwell cuBLAS GEMMs are persistent and hold every SM until they end,
-    # so a backward leaves room for concurrent bucket reduces only if its
-    # GEMMs are told to leave SMs free (the same carve-out applies to all
-    # three schedules below).
-    carve = getattr(torch._C, "_set_sm_carveout_experimental", None)
-    carveout = args.bucket_ctas if (carve is not None and args.bucket_ctas > 0) else 0
-    if carveout:
-        carve(carveout)
     out = {}
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(main):
@@ -578,16 +584,18 @@ def zero2_arm(args, w: WL.Workload):
             e1.record(main)
             torch.cuda.synchronize(dev)
             out[mode] = e0.elapsed_time(e1) / args.steps
-    if carveout:
-        carve(None)
     opt.close()
+    sms = {"bucket_group": part.sms_a, "backward_group": part.sms_b} if part else None
+    if part:
+        torch.cuda.synchronize(dev)
+        part.close()
     line = {
         "metric": "ZeRO-2 bucketed step: optimizer ms exposed after an emulated backward", "value":
             out["overlap"] - out["bwd"], "unit": "ms", "higher_is_better": False, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world, "buckets": len(cuts),
-                   "bucket_params": per_bucket, "tokens": args.tokens, "bucket_ctas": args.bucket_ctas,
-                   "gemm_sm_carveout": carveout, "backward": args.backward,
+                   "bucket_params": per_bucket, "tokens": args.tokens, "bucket_ctas": bucket_ctas,
+                   "sm_partition": sms, "backward": args.backward,
                    "bucket_update": args.bucket_update, "max_norm": hpd["max_norm"],
                    "sleep_us_per_bucket": args.sleep_us if args.backward == "sleep" else None},
         "ms": {"backward_alone": out["bwd"], "backward_then_step": out["seq"], "overlapped": out["overlap"]},
@@ -782,6 +790,8 @@ def main(argv=None):
     ap.add_argument("--bucket-mb", type=float, default=25.0, help="zero2: bucket size per rank (MB of bf16)")
     ap.add_argument("--tokens", type=int, default=8192, help="zero2: tokens of the emulated backward")
     ap.add_argument("--bucket-ctas", type=int, default=32, help="zero2: CTAs per bucket reduce (0 = one per SM)")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="zero2: SMs for the bucket reduces; the backward runs on the rest (green contexts)")
     ap.add_argument("--bucket-update", action="store_true",
                     help="zero2: clipping off; reduce and update each bucket at once (zero1_bucket_update)")
     ap.add_argument("--backward", default="gemm", choices=["gemm", "sleep"],

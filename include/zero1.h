@@ -449,6 +449,37 @@ int zero1_allreduce(uint64_t n, int world, int dtype, int op, const void *const 
 int zero1_allgather(uint64_t n, int world, uint64_t shard_len, int dtype, const void *const *shard_ptrs,
                     void *const *out_ptrs, unsigned *errors, void *stream);
 
+/* Two streams on disjoint groups of the current device's SMs, for running
+ * the bucketed step beside a backward ("Lecture 7 close reading", section
+ * 5.3; "Parallel training", "data parallel and ZeRO": communication hidden
+ * behind the backward).  The library GEMMs of a backward are persistent
+ * kernels that hold every SM until they end, so bucket reduces issued on
+ * another stream find no SM free; kernels launched on stream_a run only on
+ * the first group's SMs and kernels on stream_b only on the rest (each
+ * group is a green context of the device).  Run the backward on one stream
+ * and zero1_bucket_reduce / zero1_bucket_update on the other; order them
+ * with events as with any two streams.
+ *   sms_a: SMs wanted in the first group, 1 <= sms_a < the device's SM
+ *     count; the driver rounds it up to its partition granularity, and
+ *     sms_a / sms_b report the counts granted.
+ * The streams are cudaStream_t values passed as void*; they belong to the
+ * partition and stay valid until zero1_sm_partition_destroy, which waits
+ * for nothing: synchronize them first.  Creating a partition changes no
+ * device setting; destroying it releases its green contexts.
+ * Errors: ZERO1_EINVAL (NULL out, sms_a out of range, nothing left for
+ * the second group), ZERO1_ENODEV, ZERO1_ENOMEM, ZERO1_ECUDA (the driver
+ * has no green contexts or refused the split). */
+typedef struct zero1_sm_partition {
+    void *stream_a;
+    void *stream_b;
+    int sms_a;
+    int sms_b;
+    void *opaque;
+} zero1_sm_partition;
+
+int zero1_sm_partition_create(int sms_a, zero1_sm_partition *out);
+int zero1_sm_partition_destroy(zero1_sm_partition *part);
+
 /* Message for the last error on this thread ("" if none). */
 const char *zero1_last_error(void);
 

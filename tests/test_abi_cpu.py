@@ -132,14 +132,18 @@ def _struct_fields(name: str) -> list[tuple[str, str]]:
         if not decl:
             continue
         ctype, names = decl.split(None, 1)
-        fields += [(n.strip(), ctype) for n in names.split(",")]
+        for n in names.split(","):
+            n = n.strip()
+            fields.append((n.lstrip("*").strip(), ctype + "*" if n.startswith("*") else ctype))
     return fields
 
 
-CTYPES = {"double": C.c_double, "uint32_t": C.c_uint32, "int32_t": C.c_int32, "uint64_t": C.c_uint64}
+CTYPES = {"double": C.c_double, "uint32_t": C.c_uint32, "int32_t": C.c_int32, "uint64_t": C.c_uint64,
+          "int": C.c_int, "void*": C.c_void_p}
 
 
-@pytest.mark.parametrize("struct,binding", [("zero1_options", z._COptions), ("zero1_hparams", z._CHparams)])
+@pytest.mark.parametrize("struct,binding", [("zero1_options", z._COptions), ("zero1_hparams", z._CHparams),
+                                            ("zero1_sm_partition", z._CSmPartition)])
 def test_structs_match_header(struct, binding):
     fields = _struct_fields(struct)
     assert [n for n, _ in fields] == [n for n, _ in binding._fields_]
@@ -236,3 +240,14 @@ def test_binding_checks_pointer_counts_and_buffers(lib_path):
     with pytest.raises(ValueError, match="host memory"):
         z._check_buffer(np.zeros(16, np.uint16), 16, "bf16", True, "x")
     z._check_buffer(np.zeros(16, np.uint16), 16, "bf16", False, "x")
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_sm_partition_errors_without_a_device(lib_path):
+    with pytest.raises(z.Zero1Error) as e:
+        z.zero1_sm_partition_create(0)
+    assert e.value.code == -1
+    with pytest.raises(z.Zero1Error) as e:
+        z.zero1_sm_partition_create(16)
+    assert e.value.code == -5
+    z.zero1_sm_partition_destroy(z._CSmPartition())     # an empty partition is accepted

@@ -226,3 +226,45 @@ def test_bucket_update_errors():
         z.zero1_bucket_finish(opt.handle, None)
         torch.cuda.synchronize()
         assert opt.get_state() == 1
+
+
+def test_bucket_reduces_on_an_sm_partition():
+    """zero1_sm_partition_create splits the SMs into two green contexts; the
+    bucket reduces run on the small group's stream while bf16 GEMMs (a
+    backward's kind of work) run on the other group's stream, and the step
+    is still the oracle's bit for bit with the GPU's clip coefficient."""
+    n, world, mean = 1_000_003, 8, 4000
+    w = WL.Workload("bk_part", n, world, 0.02, 2, max_norm=0.05)
+    d = w.hparams()
+    ohp = o.HP(**d)
+    rng = np.random.default_rng(7)
+    m0 = WL.master(w, "cuda")
+    reps = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    st = o.State(f32(m0))
+    x = torch.randn(4096, 768, device="cuda", dtype=torch.bfloat16)
+    wgt = torch.randn(768, 3072, device="cuda", dtype=torch.bfloat16)
+    with z.SmPartition(16) as part:
+        total = torch.cuda.get_device_properties(0).multi_processor_count
+        assert part.sms_a >= 16 and part.sms_a + part.sms_b <= total and part.sms_b > 0
+        side = torch.cuda.ExternalStream(part.stream_a)
+        other = torch.cuda.ExternalStream(part.stream_b)
+        with z.Zero1(n, world, z.Hparams(**d), z.Options(bucket_ctas=part.sms_a)) as opt:
+            opt.set_state(m0)
+            for t in range(1, w.steps + 1):
+                grads = WL.grads(w, t, "cuda")
+                other.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(other):            # GEMMs beside the reduces
+                    ref = x @ wgt
+                    for _ in range(8):
+                        y = x @ wgt
+                _bucketed_step(opt, grads, reps, _buckets(n, rng, mean), side)
+                torch.cuda.current_stream().wait_stream(other)
+                assert torch.equal(y, ref)
+                norm, c = opt.grad_norm()
+                reps_o, norm_o, _ = o.step(st, [u16(g) for g in grads], ohp, clip_override=np.float32(c))
+                assert abs(norm - norm_o) <= 1e-6 * norm_o
+                master, m, v = _state(opt, n)
+                assert bits_equal(master, st.master) and bits_equal(m, st.m) and bits_equal(v, st.v)
+                for r in range(world):
+                    assert np.array_equal(u16(reps[r]), reps_o[r])
+        torch.cuda.synchronize()

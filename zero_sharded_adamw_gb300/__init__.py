@@ -24,6 +24,7 @@ __all__ = [
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_set_lr_ptr", "zero1_get_grad_norm",
     "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_update", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
+    "SmPartition", "zero1_sm_partition_create", "zero1_sm_partition_destroy",
     "library_path", "EXPORTED_SYMBOLS",
 ]
 
@@ -64,6 +65,8 @@ _SIGS = {
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
     "zero1_allreduce": (_I32, [_U64, _I32, _I32, _I32, _P, _P, _P, _P]),
     "zero1_allgather": (_I32, [_U64, _I32, _U64, _I32, _P, _P, _P, _P]),
+    "zero1_sm_partition_create": (_I32, [_I32, _P]),
+    "zero1_sm_partition_destroy": (_I32, [_P]),
     "zero1_last_error": (C.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -469,6 +472,45 @@ def zero1_allgather(n: int, world: int, shard_len: int, dtype: int, shard_ptrs, 
                 _check_buffer(x, own, kind, True, f"shards[{r}]")
     _check(_load().zero1_allgather(n, world, shard_len, dtype, shards, _ptrs(out_ptrs, world, n, kind, True, "out"),
                                    _addr(errors), _stream(stream)))
+
+
+class _CSmPartition(C.Structure):
+    _fields_ = [("stream_a", C.c_void_p), ("stream_b", C.c_void_p), ("sms_a", C.c_int), ("sms_b", C.c_int),
+                ("opaque", C.c_void_p)]
+
+
+def zero1_sm_partition_create(sms_a: int) -> _CSmPartition:
+    """Two streams on disjoint SM groups of the current device (green
+    contexts): the first with at least sms_a SMs, the second with the rest."""
+    part = _CSmPartition()
+    _check(_load().zero1_sm_partition_create(sms_a, C.byref(part)))
+    return part
+
+
+def zero1_sm_partition_destroy(part: _CSmPartition) -> None:
+    _check(_load().zero1_sm_partition_destroy(C.byref(part)))
+
+
+class SmPartition:
+    """Owning wrapper of zero1_sm_partition_create: ``stream_a`` / ``stream_b``
+    are the raw cudaStream_t values (wrap them with torch.cuda.ExternalStream),
+    ``sms_a`` / ``sms_b`` the SMs each group was granted."""
+
+    def __init__(self, sms_a: int):
+        self._part = zero1_sm_partition_create(sms_a)
+        self.stream_a, self.stream_b = self._part.stream_a, self._part.stream_b
+        self.sms_a, self.sms_b = self._part.sms_a, self._part.sms_b
+
+    def close(self) -> None:
+        if self._part is not None:
+            zero1_sm_partition_destroy(self._part)
+            self._part = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
 
 
 class Zero1:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libzero1.so")
-SOURCES = ["zero1_host.cu", "zero1_kernels.cu", "zero1_noalloc.cu", "zero1_allreduce.cu"]
+SOURCES = ["zero1_host.cu", "zero1_kernels.cu", "zero1_noalloc.cu", "zero1_allreduce.cu", "zero1_partition.cu"]
 HEADERS = [os.path.join(CSRC, "zero1_internal.h"), os.path.join(CSRC, "zero1_ptx.cuh"), os.path.join(INCLUDE, "zero1.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
