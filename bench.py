@@ -105,27 +105,25 @@ def _summary_fields(path: str) -> dict:
     return fields
 
 
-def kernel_traffic(workload: str) -> tuple[float | None, str | None]:
-    """DRAM bytes per launch of the update kernel from a committed ncu
-    summary taken on the current kernel source, and that summary's name:
-    the full-size one-pass capture of the workload if there is one, else a
-    small-case capture scaled to the workload's size.  (None, None) when
-    neither matches the current source."""
+def kernel_traffic(workload: str, n: int) -> tuple[float | None, str | None]:
+    """DRAM bytes per launch of the update kernel at n parameters, from the
+    committed ncu summary of the workload's recipe taken on the current
+    kernel sources: a one-kernel capture on a small case (a few GB on the
+    device), whose DRAM bytes per parameter are scaled by n (the kernel
+    streams every parameter once, so its traffic grows in proportion to n).
+    (None, None) when no summary matches the current sources."""
     sha = kernel_source_digest()
-    name = workload.replace("@", "_n")
-    for fname, key in ((f"dram_{name}.txt", "zero1_adamw_ag_kernel.dram_bytes_per_launch"),
-                       (f"zero1_adamw_ag_kernel_{name}.txt", "dram_bytes_per_launch")):
-        path = os.path.join(ROOT, "profiles", fname)
-        if not os.path.exists(path):
-            continue
-        fields = _summary_fields(path)
-        if fields.get("kernel_source_digest") != sha:
-            continue
-        try:
-            return float(fields[key]), "profiles/" + fname
-        except (KeyError, ValueError):
-            continue
-    return None, None
+    fname = f"dram_{workload.split('@')[0]}.txt"
+    path = os.path.join(ROOT, "profiles", fname)
+    if not os.path.exists(path):
+        return None, None
+    fields = _summary_fields(path)
+    if fields.get("kernel_source_digest") != sha:
+        return None, None
+    try:
+        return float(fields["zero1_adamw_ag_kernel.dram_bytes_per_param"]) * n, "profiles/" + fname
+    except (KeyError, ValueError):
+        return None, None
 
 
 class ClockSampler:
@@ -297,7 +295,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     rs_avg = rs_ms / max(1, prof_steps)
     upd_bytes = (state_rw + 2 * w.world) * w.n    # state read+write, replica writes
     rs_bytes = (2 * w.world) * w.n                # gradient reads
-    traffic, traffic_src = kernel_traffic(w.name)
+    traffic, traffic_src = kernel_traffic(w.name, w.n)
     achieved = upd_bytes / (upd_avg / 1e3) / 1e9
     launches = opt.launches_per_step()
     if launches == 1:

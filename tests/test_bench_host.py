@@ -21,20 +21,18 @@ def test_digest_ignores_comments_and_whitespace(tmp_path):
     assert bench.kernel_source_digest([str(a)]) != base
 
 
-def test_traffic_comes_only_from_summaries_of_the_current_source(tmp_path, monkeypatch):
+def test_traffic_scales_a_small_capture_of_the_current_source(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.kernel_traffic("gpt2_small") == (None, None)
+    assert bench.kernel_traffic("state_7b", 7_000_000_000) == (None, None)
     d = bench.kernel_source_digest()
-    (prof / "zero1_adamw_ag_kernel_gpt2_small.txt").write_text(
-        f"kernel_source_digest: {d}\ndram_bytes_per_launch: 123\n")
-    assert bench.kernel_traffic("gpt2_small") == (123.0, "profiles/zero1_adamw_ag_kernel_gpt2_small.txt")
-    (prof / "dram_gpt2_small.txt").write_text(
-        f"kernel_source_digest: {d}\nzero1_adamw_ag_kernel.dram_bytes_per_launch: 456\n")
-    assert bench.kernel_traffic("gpt2_small") == (456.0, "profiles/dram_gpt2_small.txt")    # full size first
-    (prof / "dram_gpt2_small.txt").write_text("kernel_source_digest: 0\nzero1_adamw_ag_kernel.dram_bytes_per_launch: 1\n")
-    assert bench.kernel_traffic("gpt2_small")[0] == 123.0                                  # stale one skipped
+    (prof / "dram_state_7b.txt").write_text(
+        f"kernel_source_digest: {d}\nzero1_adamw_ag_kernel.dram_bytes_per_param: 32.5\n")
+    assert bench.kernel_traffic("state_7b", 1000) == (32500.0, "profiles/dram_state_7b.txt")
+    assert bench.kernel_traffic("state_7b@5000", 5000)[0] == 162500.0     # a resized recipe uses its own summary
+    (prof / "dram_state_7b.txt").write_text("kernel_source_digest: 0\nzero1_adamw_ag_kernel.dram_bytes_per_param: 1\n")
+    assert bench.kernel_traffic("state_7b", 1000) == (None, None)          # taken on other sources: not used
 
 
 def test_measured_peak(tmp_path, monkeypatch):

@@ -52,6 +52,7 @@ typedef CUresult (*StreamDestroyFn)(CUstream);
 
 struct Driver {
     bool tried = false, ok = false;
+    char missing[128] = "";        // the first entry point the driver did not provide
     DeviceGetFn device_get = nullptr;
     DevResourceFn dev_resource = nullptr;
     SplitFn split = nullptr;
@@ -64,14 +65,18 @@ struct Driver {
 std::mutex g_mu;
 Driver g_drv;
 
+// The driver's entry point `name` in the version this library is built
+// against; on failure the name and the query's answer go to g_drv.missing.
 template <typename F>
-bool fetch(const char *name, unsigned version, F *out)
+bool fetch(const char *name, F *out)
 {
     void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || p == nullptr)
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion(name, &p, CUDART_VERSION, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr) {
+        snprintf(g_drv.missing, sizeof g_drv.missing, "%s (runtime %d, query %d)", name, (int)e, (int)q);
         return false;
+    }
     *out = reinterpret_cast<F>(p);
     return true;
 }
@@ -81,14 +86,14 @@ const Driver *driver()
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_drv.tried) {
         g_drv.tried = true;
-        g_drv.ok = fetch("cuDeviceGet", 12000, &g_drv.device_get) &&
-                   fetch("cuDeviceGetDevResource", 12040, &g_drv.dev_resource) &&
-                   fetch("cuDevSmResourceSplitByCount", 12040, &g_drv.split) &&
-                   fetch("cuDevResourceGenerateDesc", 12040, &g_drv.desc) &&
-                   fetch("cuGreenCtxCreate", 12040, &g_drv.green_create) &&
-                   fetch("cuGreenCtxDestroy", 12040, &g_drv.green_destroy) &&
-                   fetch("cuGreenCtxStreamCreate", 12040, &g_drv.green_stream) &&
-                   fetch("cuStreamDestroy", 12000, &g_drv.stream_destroy);
+        g_drv.ok = fetch("cuDeviceGet", &g_drv.device_get) &&
+                   fetch("cuDeviceGetDevResource", &g_drv.dev_resource) &&
+                   fetch("cuDevSmResourceSplitByCount", &g_drv.split) &&
+                   fetch("cuDevResourceGenerateDesc", &g_drv.desc) &&
+                   fetch("cuGreenCtxCreate", &g_drv.green_create) &&
+                   fetch("cuGreenCtxDestroy", &g_drv.green_destroy) &&
+                   fetch("cuGreenCtxStreamCreate", &g_drv.green_stream) &&
+                   fetch("cuStreamDestroy", &g_drv.stream_destroy);
     }
     return g_drv.ok ? &g_drv : nullptr;
 }
@@ -120,7 +125,7 @@ extern "C" int zero1_sm_partition_create(int sms_a, zero1_sm_partition *out)
     if (e != cudaSuccess) return pfail(ZERO1_ENODEV, "no CUDA device (%s)", cudaGetErrorString(e));
     if (sms_a >= total) return pfail(ZERO1_EINVAL, "sms_a = %d leaves none of the %d SMs for the second group", sms_a, total);
     const Driver *d = driver();
-    if (!d) return pfail(ZERO1_ECUDA, "the driver does not provide green contexts");
+    if (!d) return pfail(ZERO1_ECUDA, "the driver does not provide green contexts: %s", g_drv.missing);
     CUdevice dev;
     CUdevResource all{}, group{}, rest{};
     unsigned int ngroups = 1;
