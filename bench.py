@@ -243,7 +243,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     hp = z.Hparams(**w.hparams())
     opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step,
                      capturable=args.graph)
-    grad_sets = [WL.grads(w, t, dev) for t in (1, 2)]
+    grad_sets = [WL.grads(w, t, dev) for t in range(1, args.grad_sets + 1)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     opt = z.Zero1(w.n, w.world, hp, opts)
     opt.set_state(WL.master(w, dev), stream=stream)
@@ -256,7 +256,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     for i in range(args.warmup):
         if i == 0:
             w0.record(stream)
-        opt.step(grad_sets[i % 2], reps, stream)
+        opt.step(grad_sets[i % len(grad_sets)], reps, stream)
         if i == 0:
             w1.record(stream)
     torch.cuda.synchronize(dev)
@@ -272,7 +272,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     ev0.record(stream)
     h0 = time.perf_counter()
     for i in range(args.steps):
-        opt.step(tables[i % 2], rep_table, stream)
+        opt.step(tables[i % len(tables)], rep_table, stream)
     host_enqueue_s = time.perf_counter() - h0
     ev1.record(stream)
     torch.cuda.synchronize(dev)
@@ -326,7 +326,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream(dev)
             for i in range(gsteps):
-                opt.step(tables[i % 2], rep_table, cs)
+                opt.step(tables[i % len(tables)], rep_table, cs)
         for _ in range(3):
             g.replay()
         barrier(world_size)
@@ -800,6 +800,9 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--grad-sets", type=int, default=2, choices=[1, 2],
+                    help="gradient sets used in turn (2: consecutive steps never reuse inputs; 1 halves the "
+                         "device footprint, for profiler captures of one launch)")
     ap.add_argument("--moments-bf16", action="store_true", help="variant: m and v stored in bf16")
     ap.add_argument("--decay-first", action="store_true", help="variant: torch.optim.AdamW's decay order")
     ap.add_argument("--clip-eps", type=float, default=0.0, help="variant: clip eps (torch uses 1e-6)")
@@ -820,6 +823,7 @@ def main(argv=None):
            "variant": {"moments_bf16": args.moments_bf16, "decay_first": args.decay_first,
                        "clip_eps": args.clip_eps, "small_step": args.small_step, "capturable": args.graph},
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
+           "gradient_sets": args.grad_sets,
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)
                  else "working set fits in L2 (launch-latency bound)"}
     if args.path == "allreduce" and args.impl == "ours":
