@@ -242,7 +242,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
 
     hp = z.Hparams(**w.hparams())
     opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step,
-                     capturable=args.graph)
+                     capturable=args.graph, host_chunk=args.host_chunk)
     grad_sets = [WL.grads(w, t, dev) for t in range(1, args.grad_sets + 1)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     opt = z.Zero1(w.n, w.world, hp, opts)
@@ -800,6 +800,8 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--host-chunk", type=int, default=0,
+                    help="e2e: parameters per chunk of the host-buffer step (0 = the library's default)")
     ap.add_argument("--grad-sets", type=int, default=2, choices=[1, 2],
                     help="gradient sets used in turn (2: consecutive steps never reuse inputs; 1 halves the "
                          "device footprint, for profiler captures of one launch)")

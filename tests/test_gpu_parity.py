@@ -437,6 +437,45 @@ def test_step_host_chunked_against_oracle_and_buckets(world):
                 assert np.array_equal(u16(reps_d[r]), reps_i[r]), (t, r)
 
 
+@pytest.mark.parametrize("opts", [dict(moments_bf16=True), dict(decay_before_update=True, clip_eps=1e-6)])
+def test_step_host_chunked_variants_match_buckets(opts):
+    """Step variants through the chunked host path (11 chunks, the last
+    ragged) equal the device bucketed step with the same cut, bit for bit,
+    norm included, over three steps."""
+    n, world, chunk = 700_001, 4, 65_536
+    w = WL.Workload("host_var", n, world, 0.01, 3, max_norm=0.05)
+    zhp, _ = _hp(w)
+    m0 = WL.master(w, "cuda")
+    cuts = [(lo, min(chunk, n - lo)) for lo in range(0, n, chunk)]
+    mdt = torch.bfloat16 if opts.get("moments_bf16") else torch.float32
+    reps_d = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world, zhp, z.Options(host_chunk=chunk, **opts)) as a, \
+            z.Zero1(n, world, zhp, z.Options(**opts)) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, w.steps + 1):
+            g = WL.grads(w, t, "cuda")
+            hg = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True).copy_(x) for x in g]
+            hr = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+            a.step_host(hg, hr)
+            z.zero1_bucket_begin(b.handle)
+            for lo, cnt in cuts:
+                z.zero1_bucket_reduce(b.handle, lo, cnt, [x[lo:lo + cnt] for x in g])
+            z.zero1_bucket_finish(b.handle, reps_d)
+            assert a.grad_norm() == b.grad_norm()
+            sa, sb = [], []
+            for opt, out in ((a, sa), (b, sb)):
+                master = torch.empty(n, device="cuda")
+                m, v = torch.empty(n, dtype=mdt, device="cuda"), torch.empty(n, dtype=mdt, device="cuda")
+                opt.get_state(master, m, v)
+                torch.cuda.synchronize()
+                out += [master.view(torch.int32).cpu(), m.view(torch.int16 if mdt == torch.bfloat16 else torch.int32).cpu(),
+                        v.view(torch.int16 if mdt == torch.bfloat16 else torch.int32).cpu()]
+            assert all(torch.equal(x, y) for x, y in zip(sa, sb)), t
+            for r in range(world):
+                assert np.array_equal(u16(hr[r]), u16(reps_d[r])), (t, r)
+
+
 def test_step_host_async_chunked_pipelined():
     """Six pipelined host-buffer steps over 16 chunks (step t's downloads
     overlap step t+1's uploads) equal six blocking ones bit for bit, each

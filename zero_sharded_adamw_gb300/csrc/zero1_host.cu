@@ -32,8 +32,12 @@
 // Slots in each of the host path's two device rings (uploads, downloads),
 // and the copy streams each direction's chunks are dealt over (one copy
 // engine each, so that several run at once).
-constexpr int kHostSlots = 8;
-constexpr int kHostCopyStreams = 4;
+#ifndef ZERO1_HOST_SLOTS
+#define ZERO1_HOST_SLOTS 8
+#define ZERO1_HOST_COPY_STREAMS 4
+#endif
+constexpr int kHostSlots = ZERO1_HOST_SLOTS;
+constexpr int kHostCopyStreams = ZERO1_HOST_COPY_STREAMS;
 // Device bytes of one slot by default: the W ranks' bf16 slices of one chunk.
 constexpr uint64_t kHostSlotBytes = 64ull << 20;
 constexpr uint64_t kHostChunkAlign = 2048;   // chunks start on whole update tiles
