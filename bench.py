@@ -295,7 +295,8 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     rs_avg = rs_ms / max(1, prof_steps)
     upd_bytes = (state_rw + 2 * w.world) * w.n    # state read+write, replica writes
     rs_bytes = (2 * w.world) * w.n                # gradient reads
-    traffic, traffic_src = kernel_traffic(w.name, w.n)
+    # the committed captures are of the default variant (fp32 moments)
+    traffic, traffic_src = (None, None) if args.moments_bf16 else kernel_traffic(w.name, w.n)
     achieved = upd_bytes / (upd_avg / 1e3) / 1e9
     launches = opt.launches_per_step()
     if launches == 1:
