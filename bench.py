@@ -363,7 +363,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
         del tables, rep_table, grad_sets, reps
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
-        k_e2e = max(3, min(args.steps, 20))
+        k_e2e = args.e2e_steps or max(3, min(args.steps, 20))
         rates = {}
         for name in ("zero1_step_host", "zero1_step_host_async"):
             run = opt.step_host if name == "zero1_step_host" else opt.step_host_async
@@ -801,6 +801,7 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None,
                     help="override the workload's parameter count (same recipe; small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="e2e: timed steps per host entry point (0: min(steps, 20))")
     ap.add_argument("--host-chunk", type=int, default=0,
                     help="e2e: parameters per chunk of the host-buffer step (0 = the library's default)")
     ap.add_argument("--grad-sets", type=int, default=2, choices=[1, 2],

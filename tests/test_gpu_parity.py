@@ -476,6 +476,50 @@ def test_step_host_chunked_variants_match_buckets(opts):
                 assert np.array_equal(u16(hr[r]), u16(reps_d[r])), (t, r)
 
 
+def test_step_host_offsets_past_4_gib():
+    """The host-buffer step at 2.2e9 parameters (W = 2, the default chunk):
+    byte offsets into the host buffers pass 2^32.  Two steps equal the
+    device bucketed step with the same cut bit for bit (state, every
+    replica, norm)."""
+    n, world = 2_200_000_013, 2
+    free, _ = torch.cuda.mem_get_info()
+    if free < 80e9:
+        pytest.skip(f"needs ~80 GB of free device memory, {free / 1e9:.0f} GB free")
+    w = WL.Workload("host_big", n, world, 1e-3, 2)
+    zhp, _ = _hp(w)
+    cuts = None
+    reps_d = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    hg = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+    hr = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+    with z.Zero1(n, world, zhp) as a, z.Zero1(n, world, zhp) as b:
+        m0 = WL.master(w, "cuda")
+        a.set_state(m0)
+        b.set_state(m0)
+        del m0
+        for t in range(1, w.steps + 1):
+            g = WL.grads(w, t, "cuda")
+            for x, y in zip(hg, g):
+                x.copy_(y)
+            a.step_host(hg, hr)
+            if cuts is None:                        # the host path's own cut (64 MiB slots: 16M parameters at W = 2)
+                chunk = (64 << 20) // (2 * world) // 2048 * 2048
+                cuts = [(lo, min(chunk, n - lo)) for lo in range(0, n, chunk)]
+            z.zero1_bucket_begin(b.handle)
+            for lo, cnt in cuts:
+                z.zero1_bucket_reduce(b.handle, lo, cnt, [x[lo:lo + cnt] for x in g])
+            z.zero1_bucket_finish(b.handle, reps_d)
+            del g
+            assert a.grad_norm() == b.grad_norm(), t
+            for r in range(world):
+                assert torch.equal(hr[r].view(torch.int16), reps_d[r].view(torch.int16).cpu()), (t, r)
+        for lo in (0, n // 2, n - 4096):            # state on windows, including past the 4 GiB byte offset
+            xs = [np.empty(4096, np.float32) for _ in range(6)]
+            z.zero1_get_state_range(a.handle, lo, 4096, *xs[:3])
+            z.zero1_get_state_range(b.handle, lo, 4096, *xs[3:])
+            torch.cuda.synchronize()
+            assert all(bits_equal(xs[i], xs[i + 3]) for i in range(3)), lo
+
+
 def test_step_host_async_chunked_pipelined():
     """Six pipelined host-buffer steps over 16 chunks (step t's downloads
     overlap step t+1's uploads) equal six blocking ones bit for bit, each
