@@ -140,7 +140,7 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     Applies to the two-kernel path (set small_step = -1 for small n).
  *   host_chunk: parameters per chunk of the host-buffer steps
  *     (zero1_step_host, zero1_step_host_async); 0 = the default, which makes
- *     one ring slot (W ranks' bf16 slices of a chunk) 64 MiB.  Rounded down
+ *     one ring slot (W ranks' bf16 slices of a chunk) 256 MiB.  Rounded down
  *     to a multiple of 2048 (at least 2048); at most 65,536 chunks.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
@@ -193,7 +193,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
  * updated and the W replicas downloaded chunk by chunk (zero1_options
  * host_chunk) through two bounded device rings, so the device memory the
  * host path needs does not grow with n:
- *   - rings: 2 x 8 slots of W x chunk bf16 (1 GiB at the default chunk),
+ *   - rings: 2 x 8 slots of W x chunk bf16 (4 GiB at the default chunk),
  *     each direction's chunks dealt over 4 copy streams;
  *   - for W <= 2, an fp32 reduce-scatter scratch of 4*W*S bytes (the plain
  *     step re-reads the gradients instead, which the host path cannot).

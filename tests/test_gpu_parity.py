@@ -501,8 +501,8 @@ def test_step_host_offsets_past_4_gib():
             for x, y in zip(hg, g):
                 x.copy_(y)
             a.step_host(hg, hr)
-            if cuts is None:                        # the host path's own cut (64 MiB slots: 16M parameters at W = 2)
-                chunk = (64 << 20) // (2 * world) // 2048 * 2048
+            if cuts is None:                        # the host path's own cut (256 MiB slots: 64M parameters at W = 2)
+                chunk = (256 << 20) // (2 * world) // 2048 * 2048
                 cuts = [(lo, min(chunk, n - lo)) for lo in range(0, n, chunk)]
             z.zero1_bucket_begin(b.handle)
             for lo, cnt in cuts:

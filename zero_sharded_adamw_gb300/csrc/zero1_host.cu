@@ -38,8 +38,10 @@
 #endif
 constexpr int kHostSlots = ZERO1_HOST_SLOTS;
 constexpr int kHostCopyStreams = ZERO1_HOST_COPY_STREAMS;
-// Device bytes of one slot by default: the W ranks' bf16 slices of one chunk.
-constexpr uint64_t kHostSlotBytes = 64ull << 20;
+// Device bytes of one slot by default: the W ranks' bf16 slices of one chunk
+// (256 MiB: measured on GB300 hosts at 1.6-2x the host-link rate of 64 MiB
+// slots; 8 copy streams per direction with 64 MiB slots gained nothing).
+constexpr uint64_t kHostSlotBytes = 256ull << 20;
 constexpr uint64_t kHostChunkAlign = 2048;   // chunks start on whole update tiles
 
 // The host-buffer steps (zero1_step_host, zero1_step_host_async): gradients
