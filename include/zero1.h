@@ -337,7 +337,7 @@ int zero1_get_grad_norm(zero1_handle h, double *norm, float *clip_coef, void *st
 
 /* Layout facts: the shard length S, the padded state length W*S, and the
  * bytes of device memory the handle holds (state + scratch, excluding the
- * host-path staging buffers).  Any output may be NULL. */
+ * host-buffer steps' rings and scratch).  Any output may be NULL. */
 int zero1_layout(zero1_handle h, uint64_t *shard_len, uint64_t *padded_len, uint64_t *device_bytes);
 
 /* Per-kernel timing.  After zero1_profile_start, each of the next

@@ -98,9 +98,6 @@ constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_TILE, ZERO1_UPD_SPILL_BF1
                                   ZERO1_UPD_SPILL_BF16_RUNS};   // fp32 scratch, bf16 moments
 constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_TILE, ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS,
                                ZERO1_UPD_REREAD_RUNS};          // gradients re-read (W <= 2)
-#ifndef ZERO1_RS_RUNS
-#define ZERO1_RS_RUNS 0
-#endif
 constexpr int kRankGroup = 8;                    // ranks per K1 stage
 constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
 constexpr int kConsumerWarps = kConsumers / 32;
@@ -271,7 +268,7 @@ struct RsSmem {
 // in increasing order, for W < 8 a batch is `sub` consecutive tiles of the
 // CTA with all ranks.  Either way each consumer thread's fp32 sum runs over
 // the ranks strictly in order 0..W-1.
-template <int W, int CAP, bool SPILL, bool RUNS>
+template <int W, int CAP, bool SPILL>
 __global__ void __launch_bounds__(kRsThreads, 1)
 zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 {
@@ -284,15 +281,9 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
     const int sub = nw >= kRankGroup ? 1 : kRankGroup / nw;
     const uint64_t nel = p.nvec * kVec;
     const uint64_t ntiles = (nel + kTile - 1) / kTile;
-    // This CTA's tiles, i < tcta: blockIdx.x + i * gridDim.x, or (RUNS) the
-    // contiguous run [b*ntiles/G, (b+1)*ntiles/G), so that a stage's `sub`
-    // tiles are adjacent and each rank's part of them is one bulk load.
-    const uint64_t run_lo = (uint64_t)blockIdx.x * ntiles / gridDim.x;
-    const uint32_t tcta = RUNS ? (uint32_t)(((uint64_t)blockIdx.x + 1) * ntiles / gridDim.x - run_lo)
-                               : (blockIdx.x < ntiles ? (uint32_t)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u);
-    auto tile_of = [&](uint32_t i) -> uint64_t { return RUNS ? run_lo + i : blockIdx.x + (uint64_t)i * gridDim.x; };
-    // Slice of (tile q of the stage, rank r): rank-major when the tiles are adjacent.
-    auto slice = [&](int q, int r, int rn) -> int { return RUNS ? r * sub + q : q * rn + r; };
+    // This CTA's tiles: blockIdx.x + i * gridDim.x for i < tcta.
+    const uint32_t tcta = blockIdx.x < ntiles ? (uint32_t)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    auto tile_of = [&](uint32_t i) -> uint64_t { return blockIdx.x + (uint64_t)i * gridDim.x; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &sm.abort;
 
@@ -330,22 +321,14 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
                     for (int q = 0; q < sub && b * sub + q < tcta; ++q)
                         bytes += (uint32_t)rn * tile_count(nel, tile_of(b * sub + q)) * 2u;
                     mbar_arrive_expect_tx(&sm.full[s], bytes);
-                    if (RUNS) {
-                        // the stage's tiles are adjacent in memory and in shared
-                        // memory (rank-major slices): one load per rank
-                        const uint64_t base = tile_of(b * sub) * kTile;
-                        for (int r = 0; r < rn; ++r)
-                            tma_load(sm.g[s][slice(0, r, rn)], p.grads[r0 + r] + base, bytes / (uint32_t)rn, &sm.full[s]);
-                    } else {
-                        for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
-                            const uint64_t base = tile_of(b * sub + q) * kTile;
-                            const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
-                            for (int r = 0; r < rn; ++r) {
-                                if (SPILL)
-                                    tma_load_hint(sm.g[s][slice(q, r, rn)], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
-                                else
-                                    tma_load(sm.g[s][slice(q, r, rn)], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
-                            }
+                    for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
+                        const uint64_t base = tile_of(b * sub + q) * kTile;
+                        const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
+                        for (int r = 0; r < rn; ++r) {
+                            if (SPILL)
+                                tma_load_hint(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
+                            else
+                                tma_load(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
                         }
                     }
                 }
@@ -379,7 +362,7 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 #pragma unroll
                     for (int r = 0; r < kRankGroup; ++r) {
                         if (r < rn) {
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][slice(q, r, rn)][e0]);
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][q * rn + r][e0]);
                             if (grp == 0 && r == 0)
                                 set_widened(s, raw);
                             else
@@ -1090,7 +1073,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
 
     const bool spill = s.ghat != nullptr;
     if (!spill && s.world > 2) return cudaErrorInvalidValue;   // the re-read stage holds two ranks
-    auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true, false> : zero1_rs_norm_kernel<W, CAP, false, ZERO1_RS_RUNS != 0>;
+    auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
     constexpr UpdConfig U1 = kUpdSpillF32, U2 = kUpdSpillBf16, U0 = kUpdReread;
     constexpr int C1 = U1.warps, C2 = U2.warps, C0 = U0.warps;
     if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
