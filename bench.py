@@ -86,6 +86,18 @@ def reduce_max(x: float, world_size: int, device="cpu") -> float:
     return float(t.item())
 
 
+def host_available_bytes() -> int | None:
+    """Host memory available to new allocations (Linux), or None if unknown."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def measured_peak() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -354,7 +366,18 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     # the host path needs only the optimizer state, its scratch and two
     # bounded rings on the device.
     e2e = None
-    if not args.no_e2e:
+    # Every local rank pins W gradient and W replica buffers of n bf16 at
+    # once; leave the leg out (with the reason) where the node cannot hold
+    # them all, rather than exhaust its memory.
+    pinned = 4 * w.world * w.n
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", 1))
+    host_free = host_available_bytes()
+    short = host_free is not None and pinned * local_ranks > 0.8 * host_free
+    short = reduce_max(1.0 if short else 0.0, world_size, dev) > 0     # every rank takes the same branch
+    if not args.no_e2e and short:
+        e2e = {"value": None, "skipped": f"host memory: {local_ranks} rank(s) x {pinned / 1e9:.0f} GB pinned "
+                                         f"> 80% of the node's available memory"}
+    elif not args.no_e2e:
         hg = []
         for g in grad_sets[0]:
             hg.append(torch.empty(w.n, dtype=torch.bfloat16, pin_memory=True))
@@ -367,7 +390,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
         rates = {}
         for name in ("zero1_step_host", "zero1_step_host_async"):
             run = opt.step_host if name == "zero1_step_host" else opt.step_host_async
-            for _ in range(2):                     # allocates the staging buffers and streams
+            for _ in range(2):                     # sets up the rings, streams and events
                 run(hg, hr, stream)
             opt.host_sync()
             barrier(world_size)
