@@ -631,7 +631,7 @@ def test_gpt2_small_full_size_windows():
 
 
 def test_ragged_1p3b_full_size():
-    run_full_size(WL.WORKLOADS["ragged_1p3b"], steps=1)
+    run_full_size(WL.WORKLOADS["ragged_1p3b"], steps=2)
 
 
 def test_stress_w64_full_size():
@@ -644,4 +644,4 @@ def test_state_7b_full_size():
     need = (12 + 4 * w.world + 4) * w.n + (8 << 30)
     if free < need:
         pytest.skip(f"needs {need / 1e9:.0f} GB of free device memory, {free / 1e9:.0f} GB free")
-    run_full_size(w, steps=1)
+    run_full_size(w, steps=2)
