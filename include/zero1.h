@@ -434,6 +434,16 @@ int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp, uint64_t 
 int zero1_allreduce(uint64_t n, int world, int dtype, int op, const void *const *in_ptrs,
                     void *const *out_ptrs, unsigned *errors, void *stream);
 
+/* The all-reduce over a handle's W emulated ranks: zero1_allreduce(n, W,
+ * ZERO1_DTYPE_BF16, ZERO1_OP_SUM, in_ptrs, out_ptrs, NULL, stream) with the
+ * handle's n and W ("Stanford CS336 Lecture 8 close reading: Parallelism
+ * (part 2)", section 2: all-reduce = reduce-scatter + all-gather; the
+ * pages' worked example sums [0,1,2,3] + rank over 4 ranks to [6,10,14,18]).
+ * in_ptrs, out_ptrs: W device pointers to n bf16 each (16-byte aligned;
+ * out may equal in).  Touches none of the handle's optimizer state.
+ * Errors: as zero1_allreduce, and ZERO1_EINVAL for an unknown handle. */
+int zero1_allreduce_sum(zero1_handle h, const void *const *in_ptrs, void *const *out_ptrs, void *stream);
+
 /* The ZeRO-3 / FSDP parameter all-gather ("Lecture 7 close reading:
  * Parallelism (part 1)", section 5.4: before a layer runs, its sharded
  * parameters are all-gathered onto every rank; "Parallel training", "How

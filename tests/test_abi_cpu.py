@@ -175,7 +175,8 @@ def test_new_entry_points_reject_unknown_handles(lib_path):
                  lambda: z.zero1_profile_read(bogus, 4),
                  lambda: z.zero1_step_launches(bogus),
                  lambda: z.zero1_set_lr_ptr(bogus, 16),
-                 lambda: z.zero1_bucket_begin(bogus)):
+                 lambda: z.zero1_bucket_begin(bogus),
+                 lambda: z.zero1_allreduce_sum(bogus, [16], [16])):
         with pytest.raises(z.Zero1Error) as e:
             call()
         assert e.value.code == -1

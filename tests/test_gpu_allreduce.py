@@ -100,3 +100,30 @@ def test_argument_errors():
     with pytest.raises(z.Zero1Error) as e:
         z.zero1_allreduce(15, 2, z.DTYPE_F32, z.OP_SUM, [t[1:] for t in x], x)
     assert e.value.code == -2
+
+
+def test_allreduce_sum_on_a_handle():
+    """zero1_allreduce_sum takes n and W from a handle: the pages' 4-rank
+    example ([0,1,2,3] + rank -> [6,10,14,18] on every rank), and equality
+    with zero1_allreduce on a multi-tile ragged case, in place and not."""
+    x = [torch.tensor([0.0, 1, 2, 3], device="cuda").add(r).to(torch.bfloat16) for r in range(4)]
+    out = [torch.empty_like(t) for t in x]
+    with z.Zero1(4, 4) as opt:
+        z.zero1_allreduce_sum(opt.handle, x, out)
+        torch.cuda.synchronize()
+    for t in out:
+        assert t.float().tolist() == [6.0, 10.0, 14.0, 18.0]
+    n, world = 1_000_003, 8
+    g = torch.Generator(device="cuda").manual_seed(11)
+    ins = [torch.randn(n, generator=g, device="cuda").to(torch.bfloat16) for _ in range(world)]
+    want = [torch.empty_like(t) for t in ins]
+    z.zero1_allreduce(n, world, z.DTYPE_BF16, z.OP_SUM, ins, want)
+    with z.Zero1(n, world) as opt:
+        got = [torch.empty_like(t) for t in ins]
+        z.zero1_allreduce_sum(opt.handle, ins, got)
+        inplace = [t.clone() for t in ins]
+        z.zero1_allreduce_sum(opt.handle, inplace, inplace)
+        torch.cuda.synchronize()
+    for a, b, c in zip(got, want, inplace):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(c.view(torch.int16), b.view(torch.int16))

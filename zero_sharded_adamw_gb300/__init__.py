@@ -23,7 +23,7 @@ __all__ = [
     "zero1_step_host_async", "zero1_host_sync",
     "zero1_set_state", "zero1_get_state", "zero1_set_state_range", "zero1_get_state_range",
     "zero1_set_lr", "zero1_set_lr_ptr", "zero1_get_grad_norm",
-    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_update", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allgather", "zero1_last_error",
+    "zero1_layout", "zero1_bucket_begin", "zero1_bucket_reduce", "zero1_bucket_update", "zero1_bucket_finish", "zero1_profile_start", "zero1_profile_stop", "zero1_profile_read", "zero1_step_launches", "zero1_shard_plan", "zero1_step_scalars", "zero1_step_noalloc", "zero1_allreduce", "zero1_allreduce_sum", "zero1_allgather", "zero1_last_error",
     "SmPartition", "zero1_sm_partition_create", "zero1_sm_partition_destroy",
     "library_path", "EXPORTED_SYMBOLS",
 ]
@@ -64,6 +64,7 @@ _SIGS = {
     "zero1_step_scalars": (_I32, [_P, _I32, _U64, _P]),
     "zero1_step_noalloc": (_I32, [_U64, _I32, _P, _U64, _P, _P, _P, _P, _P, _P]),
     "zero1_allreduce": (_I32, [_U64, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "zero1_allreduce_sum": (_I32, [_P, _P, _P, _P]),
     "zero1_allgather": (_I32, [_U64, _I32, _U64, _I32, _P, _P, _P, _P]),
     "zero1_sm_partition_create": (_I32, [_I32, _P]),
     "zero1_sm_partition_destroy": (_I32, [_P]),
@@ -458,6 +459,13 @@ def zero1_allreduce(n: int, world: int, dtype: int, op: int, in_ptrs, out_ptrs, 
     _check(_load().zero1_allreduce(n, world, dtype, op, _ptrs(in_ptrs, world, n, kind, True, "in"),
                                    _ptrs(out_ptrs, world, n, kind, True, "out"), _addr(errors),
                                    _stream(stream)))
+
+
+def zero1_allreduce_sum(h: int, in_ptrs, out_ptrs, stream=None) -> None:
+    """bf16 sum all-reduce over the handle's W ranks of n elements each."""
+    n, world, _ = _info(h)
+    _check(_load().zero1_allreduce_sum(h, _ptrs(in_ptrs, world, n, "bf16", True, "in"),
+                                       _ptrs(out_ptrs, world, n, "bf16", True, "out"), _stream(stream)))
 
 
 def zero1_allgather(n: int, world: int, shard_len: int, dtype: int, shard_ptrs, out_ptrs, errors=None,

@@ -1089,6 +1089,13 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
     return ZERO1_OK;
 }
 
+int zero1_allreduce_sum(zero1_handle h, const void *const *in_ptrs, void *const *out_ptrs, void *stream)
+{
+    if (!live(h)) return fail(ZERO1_EINVAL, "invalid handle");
+    DeviceGuard g(h->device);
+    return zero1_allreduce(h->n, h->world, ZERO1_DTYPE_BF16, ZERO1_OP_SUM, in_ptrs, out_ptrs, nullptr, stream);
+}
+
 int zero1_shard_plan(uint64_t n, int world, uint64_t *shard_len, uint64_t *padded_len)
 {
     if (n == 0) return fail(ZERO1_EINVAL, "n must be > 0");
