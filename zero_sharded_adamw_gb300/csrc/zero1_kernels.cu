@@ -48,7 +48,32 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTile = 2048;                      // parameters per tile
+// The reduce-scatter kernel's tiles, per path: each rank's slice of a tile
+// is one bulk load of tile * 2 bytes, a stage holds `ranks` ranks' slices of
+// one tile, and `stages` stages are in flight.  The size of each bulk copy
+// sets the read rate (measured on GB300 with 152 CTAs streaming 8 GiB:
+// 7.43-7.54 TB/s in 16 KB copies, 6.20 TB/s in 4 KB copies).  Measured
+// per path in interleaved repeats on one box:
+//  - gradients only read (W <= 2): 8192-parameter tiles, 2 ranks per stage
+//    (16 KB copies, 128 KB in flight): the 7B step's reduce 4.23 -> 3.77 ms
+//    against 2048-parameter tiles of 4 tiles x 2 ranks per stage;
+//  - fp32 scratch written (W >= 3): 4096-parameter tiles, 4 ranks per stage
+//    (8 KB copies), 0.1-0.4% faster than 2048 x 8 ranks and than 8192 x 2.
+struct RsConfig {
+    int tile, ranks, stages;
+};
+#ifndef ZERO1_RS_SPILL_TILE
+#define ZERO1_RS_SPILL_TILE 4096
+#define ZERO1_RS_SPILL_RANKS 4
+#define ZERO1_RS_SPILL_STAGES 4
+#endif
+#ifndef ZERO1_RS_READ_TILE
+#define ZERO1_RS_READ_TILE 8192
+#define ZERO1_RS_READ_RANKS 2
+#define ZERO1_RS_READ_STAGES 4
+#endif
+constexpr RsConfig kRsSpill{ZERO1_RS_SPILL_TILE, ZERO1_RS_SPILL_RANKS, ZERO1_RS_SPILL_STAGES};
+constexpr RsConfig kRsRead{ZERO1_RS_READ_TILE, ZERO1_RS_READ_RANKS, ZERO1_RS_READ_STAGES};
 // 1: whole steps launch their two kernels with programmatic dependencies
 // (programmatic dependent launch).  Off by default: measured in 50-step CUDA
 // graphs on GB300 it was mixed -- 7% faster at 65,536 parameters (W = 4),
@@ -56,7 +81,6 @@ constexpr int kTile = 2048;                      // parameters per tile
 #ifndef ZERO1_PDL
 #define ZERO1_PDL 0
 #endif
-constexpr int kStages = 4;                       // shared-memory ring depth, reduce-scatter kernel (3 and 2 measured slower)
 // The update kernel's tile, ring depth, consumer warps and tile order, per
 // path (measured on GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment
 // workloads):
@@ -98,11 +122,11 @@ constexpr UpdConfig kUpdSpillBf16{ZERO1_UPD_SPILL_BF16_TILE, ZERO1_UPD_SPILL_BF1
                                   ZERO1_UPD_SPILL_BF16_RUNS};   // fp32 scratch, bf16 moments
 constexpr UpdConfig kUpdReread{ZERO1_UPD_REREAD_TILE, ZERO1_UPD_REREAD_STAGES, ZERO1_UPD_REREAD_WARPS,
                                ZERO1_UPD_REREAD_RUNS};          // gradients re-read (W <= 2)
-constexpr int kRankGroup = 8;                    // ranks per K1 stage
-constexpr int kConsumers = 256;                  // 8 warps x 8 parameters = kTile
+constexpr int kConsumers = 256;                  // consumer threads of the reduce-scatter kernel
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kRsThreads = kConsumers + 32;      // + producer warp
-static_assert(kConsumers * kVec == kTile, "one 8-parameter vector per consumer thread");
+static_assert(kRsSpill.tile % (kConsumers * kVec) == 0 && kRsRead.tile % (kConsumers * kVec) == 0,
+              "consumers must tile the reduce-scatter tiles");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
@@ -247,40 +271,43 @@ __device__ __forceinline__ StepScalars form_scalars(const StepScalars &base, con
 
 // ------------------------------------------------------------------- K1
 
-// Parameters of tile j that lie in the 8-aligned vector part [0, nel).
-__device__ __forceinline__ uint32_t tile_count(uint64_t nel, uint64_t j)
+// Parameters of tile j (of `tile` parameters) that lie in the 8-aligned
+// vector part [0, nel).
+__device__ __forceinline__ uint32_t rs_tile_count(uint64_t nel, uint64_t j, uint64_t tile)
 {
-    const uint64_t base = j * kTile;
-    return (uint32_t)(nel - base < (uint64_t)kTile ? nel - base : kTile);
+    const uint64_t base = j * tile;
+    return (uint32_t)(nel - base < tile ? nel - base : tile);
 }
 
+template <int TILE, int RANKS, int STAGES>
 struct RsSmem {
-    uint16_t g[kStages][kRankGroup][kTile];   // 128 KB: eight 4 KB (rank, tile) slices per stage
-    uint64_t full[kStages], empty[kStages];
+    uint16_t g[STAGES][RANKS][TILE];   // 128 KB: RANKS (rank, tile) slices per stage
+    uint64_t full[STAGES], empty[STAGES];
     double red_a[kConsumerWarps], red_b[kConsumerWarps];
     int abort;
     int last;
 };
 
 // Warps 0..7 consume, warp 8 produces.  A CTA's tiles are j = blockIdx.x,
-// +gridDim.x, ... in increasing order; work item k of a CTA is (batch b,
-// rank group grp): for W >= 8 a batch is one tile and its rank groups come
-// in increasing order, for W < 8 a batch is `sub` consecutive tiles of the
-// CTA with all ranks.  Either way each consumer thread's fp32 sum runs over
-// the ranks strictly in order 0..W-1.
+// +gridDim.x, ... in increasing order; work item k of a CTA is (tile, rank
+// group grp), the rank groups of a tile in increasing order, so each
+// consumer thread's fp32 sums run over the ranks strictly in order 0..W-1.
+// Consumer thread t owns the 8-parameter vectors q * 2048 + 8 t (q <
+// tile / 2048) of every tile: a warp's 16-byte shared-memory reads are
+// consecutive.
 template <int W, int CAP, bool SPILL>
 __global__ void __launch_bounds__(kRsThreads, 1)
 zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
 {
+    constexpr RsConfig kCfg = SPILL ? kRsSpill : kRsRead;
+    constexpr int kRsTile = kCfg.tile, kRsRanks = kCfg.ranks, kStages = kCfg.stages;
+    constexpr int kRsVecs = kRsTile / (kConsumers * kVec);   // 8-parameter vectors per consumer thread per tile
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    RsSmem &sm = *reinterpret_cast<RsSmem *>(smem_raw);
+    RsSmem<kRsTile, kRsRanks, kStages> &sm = *reinterpret_cast<RsSmem<kRsTile, kRsRanks, kStages> *>(smem_raw);
     const int nw = W > 0 ? W : p.world;
-    // A stage holds eight 4 KB (rank, tile) slices: one rank group of one
-    // tile when W >= 8, else `sub` whole tiles of all W ranks.
-    const int ngroups = (nw + kRankGroup - 1) / kRankGroup;
-    const int sub = nw >= kRankGroup ? 1 : kRankGroup / nw;
+    const int ngroups = (nw + kRsRanks - 1) / kRsRanks;
     const uint64_t nel = p.nvec * kVec;
-    const uint64_t ntiles = (nel + kTile - 1) / kTile;
+    const uint64_t ntiles = (nel + kRsTile - 1) / kRsTile;
     // This CTA's tiles: blockIdx.x + i * gridDim.x for i < tcta.
     const uint32_t tcta = blockIdx.x < ntiles ? (uint32_t)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
     auto tile_of = [&](uint32_t i) -> uint64_t { return blockIdx.x + (uint64_t)i * gridDim.x; };
@@ -310,26 +337,21 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
             // update kernel re-reads the gradients they keep normal priority.
             const uint64_t pol = SPILL ? policy_evict_first() : 0;
             uint32_t k = 0;
-            for (uint32_t b = 0; b * sub < tcta && !*abort; ++b) {
+            for (uint32_t i = 0; i < tcta && !*abort; ++i) {
+                const uint64_t base = tile_of(i) * kRsTile;
+                const uint32_t cnt = rs_tile_count(nel, tile_of(i), kRsTile);
                 for (int grp = 0; grp < ngroups; ++grp, ++k) {
                     const int s = k % kStages;
                     if (k >= kStages && !mbar_wait(&sm.empty[s], ((k / kStages) & 1u) ^ 1u, abort, &p.status->errors))
                         break;
-                    const int r0 = grp * kRankGroup;
-                    const int rn = nw - r0 < kRankGroup ? nw - r0 : kRankGroup;
-                    uint32_t bytes = 0;
-                    for (int q = 0; q < sub && b * sub + q < tcta; ++q)
-                        bytes += (uint32_t)rn * tile_count(nel, tile_of(b * sub + q)) * 2u;
-                    mbar_arrive_expect_tx(&sm.full[s], bytes);
-                    for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
-                        const uint64_t base = tile_of(b * sub + q) * kTile;
-                        const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
-                        for (int r = 0; r < rn; ++r) {
-                            if (SPILL)
-                                tma_load_hint(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
-                            else
-                                tma_load(sm.g[s][q * rn + r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
-                        }
+                    const int r0 = grp * kRsRanks;
+                    const int rn = nw - r0 < kRsRanks ? nw - r0 : kRsRanks;
+                    mbar_arrive_expect_tx(&sm.full[s], (uint32_t)rn * cnt * 2u);
+                    for (int r = 0; r < rn; ++r) {
+                        if (SPILL)
+                            tma_load_hint(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s], pol);
+                        else
+                            tma_load(sm.g[s][r], p.grads[r0 + r] + base, cnt * 2u, &sm.full[s]);
                     }
                 }
             }
@@ -338,14 +360,15 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
         return;
     }
 
-    // Consumers: thread t owns parameters [8t, 8t+8) of every tile.
+    // Consumers.
     Kahan acc;
     const uint64_t keep = policy_evict_last();
-    const uint32_t e0 = threadIdx.x * kVec;
     uint32_t k = 0;
-    float s[8];
-    for (uint32_t b = 0; b * sub < tcta; ++b) {
+    float s[kRsVecs][8];
+    for (uint32_t i = 0; i < tcta; ++i) {
         if (__any_sync(0xFFFFFFFFu, *abort != 0)) break;
+        const uint64_t base = tile_of(i) * kRsTile;
+        const uint32_t cnt = rs_tile_count(nel, tile_of(i), kRsTile);
         bool ok = true;
         for (int grp = 0; grp < ngroups; ++grp, ++k) {
             const int st = k % kStages;
@@ -354,25 +377,25 @@ zero1_rs_norm_kernel(const __grid_constant__ RsParams<CAP> p)
                 ok = false;
                 break;
             }
-            const int rn = nw - grp * kRankGroup < kRankGroup ? nw - grp * kRankGroup : kRankGroup;
-            for (int q = 0; q < sub && b * sub + q < tcta; ++q) {
-                const uint64_t base = tile_of(b * sub + q) * kTile;
-                const uint32_t cnt = tile_count(nel, tile_of(b * sub + q));
+            const int rn = nw - grp * kRsRanks < kRsRanks ? nw - grp * kRsRanks : kRsRanks;
+#pragma unroll
+            for (int q = 0; q < kRsVecs; ++q) {
+                const uint32_t e0 = (uint32_t)q * (kConsumers * kVec) + threadIdx.x * kVec;
                 if (e0 < cnt) {
 #pragma unroll
-                    for (int r = 0; r < kRankGroup; ++r) {
+                    for (int r = 0; r < kRsRanks; ++r) {
                         if (r < rn) {
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][q * rn + r][e0]);
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.g[st][r][e0]);
                             if (grp == 0 && r == 0)
-                                set_widened(s, raw);
+                                set_widened(s[q], raw);
                             else
-                                add_widened(s, raw);
+                                add_widened(s[q], raw);
                         }
                     }
-                    if (grp == ngroups - 1) {          // all W ranks summed: finish the tile
+                    if (grp == ngroups - 1) {          // all W ranks summed: finish the vector
                         float g[8];
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) g[c8] = __fmul_rn(s[c8], p.inv_w);
+                        for (int c8 = 0; c8 < 8; ++c8) g[c8] = __fmul_rn(s[q][c8], p.inv_w);
                         if (SPILL) {
                             st_hint(p.ghat + base + e0, make_float4(g[0], g[1], g[2], g[3]), keep);
                             st_hint(p.ghat + base + e0 + 4, make_float4(g[4], g[5], g[6], g[7]), keep);
@@ -1076,7 +1099,9 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     auto k1 = spill ? zero1_rs_norm_kernel<W, CAP, true> : zero1_rs_norm_kernel<W, CAP, false>;
     constexpr UpdConfig U1 = kUpdSpillF32, U2 = kUpdSpillBf16, U0 = kUpdReread;
     constexpr int C1 = U1.warps, C2 = U2.warps, C0 = U0.warps;
-    if ((e = allow_smem(k1, sizeof(RsSmem))) != cudaSuccess) return e;
+    const size_t k1_smem = spill ? sizeof(RsSmem<kRsSpill.tile, kRsSpill.ranks, kRsSpill.stages>)
+                                 : sizeof(RsSmem<kRsRead.tile, kRsRead.ranks, kRsRead.stages>);
+    if ((e = allow_smem(k1, k1_smem)) != cudaSuccess) return e;
     const int path = spill ? (s.moments_bf16 ? 2 : 1) : 0;
     auto k2 = path == 1   ? zero1_adamw_ag_kernel<W, CAP, false, false, U1.tile, U1.stages, C1, U1.runs>
               : path == 2 ? zero1_adamw_ag_kernel<W, CAP, false, true, U2.tile, U2.stages, C2, U2.runs>
@@ -1098,7 +1123,7 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
     cudaLaunchConfig_t c1 = {};
     c1.gridDim = dim3(s.grid_rs);
     c1.blockDim = dim3(kRsThreads);
-    c1.dynamicSmemBytes = sizeof(RsSmem);
+    c1.dynamicSmemBytes = k1_smem;
     c1.stream = stream;
     c1.attrs = attr;
     c1.numAttrs = pdl ? 1 : 0;
@@ -1138,7 +1163,8 @@ void plan_grids(uint64_t n, bool reread, int num_sms, int *grid_rs, int *grid_up
     // Persistent kernels: one CTA per SM (each holds ~130-220 KB of shared
     // memory), never more CTAs than tiles, at least one (the n % 8 tail).
     // The update kernel's tile depends on its path (re-read or scratch).
-    const uint64_t ntiles = (n / kVec * kVec + kTile - 1) / kTile;
+    const uint64_t rs_tile = (uint64_t)(reread ? kRsRead.tile : kRsSpill.tile);
+    const uint64_t ntiles = (n / kVec * kVec + rs_tile - 1) / rs_tile;
     uint64_t g = (uint64_t)num_sms;
     if (ntiles < g) g = ntiles;
     if (g < 1) g = 1;
