@@ -22,11 +22,11 @@
 //
 // Both kernels are HBM streams (no contraction, so no tensor cores) built as
 // persistent, warp-specialised TMA pipelines, one CTA per SM:
-//  - a producer warp moves 2048-parameter tiles from HBM into a 4-stage
+//  - a producer warp moves tiles (2048-8192 parameters, per kernel and
+//    path; see the configurations below) from HBM into a 3-4 stage
 //    shared-memory ring with 1-D bulk copies (cp.async.bulk) that complete
 //    on an mbarrier per stage;
-//  - 8 consumer warps (8 parameters per thread per tile) compute out of
-//    shared memory;
+//  - 8 or 16 consumer warps compute out of shared memory;
 //  - K2 has a store warp whose lanes write the tile's master, m, v and W
 //    bf16 replicas back with bulk stores, so the W-way all-gather costs the
 //    SM one bulk instruction per replica per tile.
