@@ -98,6 +98,16 @@ def host_available_bytes() -> int | None:
     return None
 
 
+def host_memory_short(pinned_per_rank: int, local_ranks: int, world_size: int, device="cpu",
+                      available: int | None = None) -> bool:
+    """True on every rank if any rank's node cannot pin `local_ranks` x
+    pinned_per_rank bytes within 80% of its available memory (collective,
+    so that all ranks take the same branch)."""
+    avail = host_available_bytes() if available is None else available
+    short = avail is not None and pinned_per_rank * local_ranks > 0.8 * avail
+    return reduce_max(1.0 if short else 0.0, world_size, device) > 0
+
+
 def measured_peak() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -371,9 +381,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
     # them all, rather than exhaust its memory.
     pinned = 4 * w.world * w.n
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", 1))
-    host_free = host_available_bytes()
-    short = host_free is not None and pinned * local_ranks > 0.8 * host_free
-    short = reduce_max(1.0 if short else 0.0, world_size, dev) > 0     # every rank takes the same branch
+    short = host_memory_short(pinned, local_ranks, world_size, dev)
     if not args.no_e2e and short:
         e2e = {"value": None, "skipped": f"host memory: {local_ranks} rank(s) x {pinned / 1e9:.0f} GB pinned "
                                          f"> 80% of the node's available memory"}

@@ -23,8 +23,10 @@ def _rank_main(rank: int, world: int, port: int, q):
     bench.init_dist(ws, "gloo")
     bench.barrier(ws)
     got = bench.reduce_max(10.0 + 5.0 * rank, ws)
+    # rank 1's node is short of host memory, rank 0's is not: both skip
+    short = bench.host_memory_short(1 << 30, 2, ws, available=(1 << 40) if rank == 0 else (1 << 20))
     bench.barrier(ws)
-    q.put((r, ws, lr, got))
+    q.put((r, ws, lr, got, short))
     torch.distributed.destroy_process_group()
 
 
@@ -41,8 +43,11 @@ def test_two_gloo_ranks_take_the_max_time():
     results = sorted(q.get(timeout=5) for _ in range(world))
     assert [r[0] for r in results] == [0, 1]
     assert all(r[1] == world and r[3] == 15.0 for r in results)
+    assert all(r[4] for r in results)           # the host-memory check is collective
 
 
 def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.5, 1) == 3.5
+    assert not bench.host_memory_short(1 << 30, 1, 1, available=1 << 40)
+    assert bench.host_memory_short(1 << 30, 8, 1, available=8 << 30)
