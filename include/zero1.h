@@ -474,8 +474,10 @@ int zero1_allgather(uint64_t n, int world, uint64_t shard_len, int dtype, const 
  *     sms_a / sms_b report the counts granted.
  * The streams are cudaStream_t values passed as void*; they belong to the
  * partition and stay valid until zero1_sm_partition_destroy, which waits
- * for nothing: synchronize them first.  Creating a partition changes no
- * device setting; destroying it releases its green contexts.
+ * for the work queued on both to finish and then releases the green
+ * contexts (ZERO1_ECUDA if that wait fails; the partition is released and
+ * *part cleared either way).  Creating a partition changes no device
+ * setting.
  * Errors: ZERO1_EINVAL (NULL out, sms_a out of range, nothing left for
  * the second group), ZERO1_ENODEV, ZERO1_ENOMEM, ZERO1_ECUDA (the driver
  * has no green contexts or refused the split). */

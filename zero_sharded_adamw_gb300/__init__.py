@@ -510,9 +510,10 @@ class SmPartition:
         self.sms_a, self.sms_b = self._part.sms_a, self._part.sms_b
 
     def close(self) -> None:
+        """Wait for both streams' work, then release the green contexts."""
         if self._part is not None:
-            zero1_sm_partition_destroy(self._part)
-            self._part = None
+            part, self._part = self._part, None
+            zero1_sm_partition_destroy(part)
 
     def __enter__(self):
         return self

@@ -163,7 +163,18 @@ extern "C" int zero1_sm_partition_destroy(zero1_sm_partition *part)
     if (!part || !part->opaque) return ZERO1_OK;
     const Driver *d = driver();
     if (!d) return pfail(ZERO1_ECUDA, "the driver does not provide green contexts");
-    release(d, static_cast<Partition *>(part->opaque));
+    Partition *p = static_cast<Partition *>(part->opaque);
+    // Work still queued on either stream finishes before its green context
+    // goes away; a failed wait is reported, and the partition released all
+    // the same.
+    cudaError_t werr = cudaSuccess;
+    for (int i = 0; i < 2; ++i) {
+        const cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(p->stream[i]));
+        if (e != cudaSuccess && werr == cudaSuccess) werr = e;
+    }
+    release(d, p);
     *part = zero1_sm_partition{};
+    if (werr != cudaSuccess)
+        return pfail(ZERO1_ECUDA, "waiting for the partition's streams failed: %s", cudaGetErrorString(werr));
     return ZERO1_OK;
 }
