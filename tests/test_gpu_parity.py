@@ -555,6 +555,47 @@ def test_step_host_async_chunked_pipelined():
         assert all(np.array_equal(a, b) for a, b in zip(reps, reps0))
 
 
+@pytest.mark.parametrize("n,world,chunk", [(1, 1, 0), (2047, 3, 0), (5000, 64, 2048), (130_001, 8, 0)])
+def test_step_host_edge_shapes(n, world, chunk):
+    """The host-buffer step at the shapes the other host tests leave out:
+    one parameter on one rank, n below one chunk (the default chunk, or
+    2048 parameters at W = 64, so three chunks with a ragged last one),
+    W = 64.  Two steps: state and every replica bit for bit the oracle's
+    with the step's clip coefficient injected, the norm within 1e-6 of the
+    oracle's, and norm and replicas equal to the device bucketed step with
+    the host path's cut."""
+    w = WL.Workload(f"host_edge_{n}_{world}", n, world, 0.01, 2, max_norm=0.05)
+    zhp, ohp = _hp(w)
+    m0 = WL.master(w, "cuda")
+    step = chunk or n
+    cuts = [(lo, min(step, n - lo)) for lo in range(0, n, step)]
+    inj = o.State(f32(m0))
+    reps_d = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    with z.Zero1(n, world, zhp, z.Options(host_chunk=chunk)) as a, z.Zero1(n, world, zhp) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, w.steps + 1):
+            g = WL.grads(w, t, "cuda")
+            hg = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True).copy_(x) for x in g]
+            hr = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(world)]
+            a.step_host(hg, hr)
+            norm_a, c_a = a.grad_norm()
+            z.zero1_bucket_begin(b.handle)
+            for lo, cnt in cuts:
+                z.zero1_bucket_reduce(b.handle, lo, cnt, [x[lo:lo + cnt] for x in g])
+            z.zero1_bucket_finish(b.handle, reps_d)
+            assert (norm_a, c_a) == b.grad_norm(), t
+            reps_i, norm_i, _ = o.step(inj, [u16(x) for x in g], ohp, clip_override=np.float32(c_a))
+            assert abs(norm_a - norm_i) <= TOL * norm_i
+            sa = _state(a, n)
+            assert sa[3] == t
+            for x, ref in zip(sa[:3], (inj.master, inj.m, inj.v)):
+                assert bits_equal(x, ref), t
+            for r in range(world):
+                assert np.array_equal(u16(hr[r]), reps_i[r]), (t, r)
+                assert np.array_equal(u16(reps_d[r]), reps_i[r]), (t, r)
+
+
 # --------------------------------------------------------- full sizes
 
 def _windows(n: int, world: int, shard: int, rng, width=4096, n_random=8):
