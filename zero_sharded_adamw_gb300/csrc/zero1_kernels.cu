@@ -58,7 +58,10 @@ using namespace ptx;
 //    (16 KB copies, 128 KB in flight): the 7B step's reduce 4.23 -> 3.77 ms
 //    against 2048-parameter tiles of 4 tiles x 2 ranks per stage;
 //  - fp32 scratch written (W >= 3): 4096-parameter tiles, 4 ranks per stage
-//    (8 KB copies), 0.1-0.4% faster than 2048 x 8 ranks and than 8192 x 2.
+//    (8 KB copies), 0.1-0.4% faster than 2048 x 8 ranks and than 8192 x 2;
+//    8192 x 1 x 8 stages and 8192 x 4 x 3 are 1-3% slower, and deeper rings
+//    (192 KB in flight: 8192 x 2 x 6, 4096 x 4 x 6, 16384 x 1 x 6) 3-8%
+//    slower, at W = 8 and at W = 64 alike.
 struct RsConfig {
     int tile, ranks, stages;
 };
