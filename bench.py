@@ -264,7 +264,7 @@ def ours_arm(args, w: WL.Workload, cfg: dict):
 
     hp = z.Hparams(**w.hparams())
     opts = z.Options(args.decay_first, args.clip_eps, args.moments_bf16, small_step=args.small_step,
-                     capturable=args.graph, host_chunk=args.host_chunk)
+                     capturable=args.graph, host_chunk=args.host_chunk, load_phase_gbs=args.load_phase_gbs)
     grad_sets = [WL.grads(w, t, dev) for t in range(1, args.grad_sets + 1)]
     reps = [torch.empty(w.n, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
     opt = z.Zero1(w.n, w.world, hp, opts)
@@ -841,6 +841,8 @@ def main(argv=None):
     ap.add_argument("--moments-bf16", action="store_true", help="variant: m and v stored in bf16")
     ap.add_argument("--decay-first", action="store_true", help="variant: torch.optim.AdamW's decay order")
     ap.add_argument("--clip-eps", type=float, default=0.0, help="variant: clip eps (torch uses 1e-6)")
+    ap.add_argument("--load-phase-gbs", type=float, default=0.0,
+                    help="update-kernel load phasing: 0 = built-in rule, > 0 = device-wide rate in GB/s, < 0 = off")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="capturable handle; also time steps captured in a CUDA graph and replayed")
@@ -856,7 +858,8 @@ def main(argv=None):
     cfg = {"workload": w.name, "n_params": w.n, "emulated_ranks": w.world,
            "bytes_per_param": 4 * w.world + (16 if args.moments_bf16 else 24), "hparams": w.hparams(),
            "variant": {"moments_bf16": args.moments_bf16, "decay_first": args.decay_first,
-                       "clip_eps": args.clip_eps, "small_step": args.small_step, "capturable": args.graph},
+                       "clip_eps": args.clip_eps, "small_step": args.small_step, "capturable": args.graph,
+                       "load_phase_gbs": args.load_phase_gbs},
            "parallelism": f"zero1 over {w.world} emulated ranks per GPU; GPUs run independent replicas",
            "gradient_sets": args.grad_sets,
            "l2": "inputs larger than L2 (no flush)" if w.bytes_per_step() > 4 * (126 << 20)

@@ -142,6 +142,23 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     (zero1_step_host, zero1_step_host_async); 0 = the default, which makes
  *     one ring slot (W ranks' bf16 slices of a chunk) 256 MiB.  Rounded down
  *     to a multiple of 2048 (at least 2048); at most 65,536 chunks.
+ *   load_phase_gbs: load phasing of the update kernel.  Where the replica
+ *     stores far outweigh the loads (the fp32-scratch step with fp32
+ *     moments at 24 <= W <= 64: 16 bytes loaded against 12 + 2W stored per
+ *     parameter), loads issued one tile at a time by each SM reach DRAM
+ *     scattered among the stores and cost more than their bytes.  Phased,
+ *     each CTA issues a tile's loads only at the next boundary of a period
+ *     that every SM shares (the global nanosecond clock), so the grid's
+ *     loads arrive together (measured on GB300 at 100M parameters: the
+ *     update 11.6% faster at W = 64, 9.1% at W = 48, 5.8% at W = 32, 3.9%
+ *     at W = 24; at W = 16 and below it is slower, so it stays off).  The
+ *     period is the time one tile's bytes take when the grid moves them at
+ *     a device-wide rate: 0 = the built-in rate (6800 GB/s up to W = 32,
+ *     rising to 7100 at W = 64; phasing off outside 24 <= W <= 64), > 0 =
+ *     this rate in GB/s for any W on that path, < 0 = never.  Only launches
+ *     whose grid spans every SM are phased (not zero1_bucket_update with
+ *     bucket_ctas, nor small pieces).  Timing only: results are the same
+ *     bit for bit.  Must be finite.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -153,13 +170,14 @@ typedef struct zero1_options {
     int32_t capturable;
     int32_t inject_wait_timeout;
     uint64_t host_chunk;
+    double load_phase_gbs;
 } zero1_options;
 
 /* zero1_create with step variants (opts may be NULL: the default step).
  * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
  * negative or non-finite clip_eps, a negative bucket_ctas, small_step
- * outside {-1, 0, 1}, capturable or inject_wait_timeout outside {0, 1}, and
- * a capturable handle whose bias corrections would need more than 2^22
+ * outside {-1, 0, 1}, capturable or inject_wait_timeout outside {0, 1}, a
+ * non-finite load_phase_gbs, and a capturable handle whose bias corrections would need more than 2^22
  * table entries.  All option checks come before any device call. */
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
                     zero1_handle *out);

@@ -156,13 +156,15 @@ def test_options_checked_before_the_device(lib_path):
     """Valid options pass the checks (the call then finds no device); a wrong
     size or an out-of-range field is rejected first."""
     with pytest.raises(z.Zero1Error) as e:
-        z.zero1_create_ex(4096, 4, None, z.Options(capturable=True, small_step=-1, moments_bf16=True))
+        z.zero1_create_ex(4096, 4, None, z.Options(capturable=True, small_step=-1, moments_bf16=True,
+                                                   load_phase_gbs=-1.0))
     assert e.value.code == -5
     lib = z._load()
     hp = z.Hparams()._c()
     h = C.c_void_p()
     for field, value in (("size", 8), ("small_step", 2), ("capturable", 3), ("inject_wait_timeout", 2),
-                         ("bucket_ctas", -1), ("clip_eps", -1.0)):
+                         ("bucket_ctas", -1), ("clip_eps", -1.0), ("load_phase_gbs", float("nan")),
+                         ("load_phase_gbs", float("inf"))):
         opts = z.Options()._c()
         setattr(opts, field, value)
         assert lib.zero1_create_ex(4096, 4, C.byref(hp), C.byref(opts), C.byref(h)) == -1, field

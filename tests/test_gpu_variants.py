@@ -180,3 +180,38 @@ def test_bf16_moments_range_checkpoint():
         resumed = _moments(c, n, True)
     for x, y in zip(full, resumed):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+@pytest.mark.parametrize("world,rate", [(24, 0.0), (64, 0.0), (8, 6500.0)])
+def test_load_phasing_is_timing_only(world, rate):
+    """The update kernel with phased loads (the built-in rule at W = 24 and
+    W = 64, an explicit device-wide rate at W = 8; 1M parameters, so the
+    grid spans every SM) computes what the free-running kernel computes, bit
+    for bit, and what the oracle computes with the step's clip coefficient
+    injected, over three steps."""
+    n = 1_000_003
+    w = WL.Workload(f"phase_w{world}", n, world, 1e-3, 3, max_norm=0.5, rank_mean_step=1e-5)
+    d = w.hparams()
+    ohp = o.HP(**d)
+    m0 = WL.master(w, "cuda")
+    grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    ra = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    rb = [torch.empty_like(x) for x in ra]
+    inj = o.State(f32(m0))
+    with z.Zero1(n, world, z.Hparams(**d), z.Options(load_phase_gbs=rate)) as a, \
+            z.Zero1(n, world, z.Hparams(**d), z.Options(load_phase_gbs=-1.0)) as b:
+        a.set_state(m0)
+        b.set_state(m0)
+        for t in range(1, 4):
+            WL.grads(w, t, "cuda", out=grads)
+            a.step(grads, ra)
+            b.step(grads, rb)
+            norm_a, c_a = a.grad_norm()
+            assert (norm_a, c_a) == b.grad_norm(), t
+            reps_i, _, _ = o.step(inj, [u16(g) for g in grads], ohp, clip_override=np.float32(c_a))
+            sa, sb = _moments(a, n, False), _moments(b, n, False)
+            for x, y, ref in zip(sa, sb, (inj.master, inj.m, inj.v)):
+                assert bits_equal(x, ref) and bits_equal(y, ref), t
+            for r in range(world):
+                assert np.array_equal(u16(ra[r]), reps_i[r]), (t, r)
+                assert np.array_equal(u16(rb[r]), reps_i[r]), (t, r)

@@ -109,7 +109,8 @@ class Hparams:
 class _COptions(C.Structure):
     _fields_ = [("size", C.c_uint32), ("decay_before_update", C.c_int32), ("clip_eps", C.c_double),
                 ("moments_bf16", C.c_int32), ("bucket_ctas", C.c_int32), ("small_step", C.c_int32),
-                ("capturable", C.c_int32), ("inject_wait_timeout", C.c_int32), ("host_chunk", C.c_uint64)]
+                ("capturable", C.c_int32), ("inject_wait_timeout", C.c_int32), ("host_chunk", C.c_uint64),
+                ("load_phase_gbs", C.c_double)]
 
 
 @dataclass
@@ -118,7 +119,8 @@ class Options:
     clip_grad_norm_ uses 1e-6), m and v stored in bf16; the bucketed step's
     CTAs per bucket; the one-launch small-n path (0 auto, 1 on, -1 off);
     capturable steps (device-side step counter and lr, for CUDA graphs);
-    the host-buffer steps' chunk size."""
+    the host-buffer steps' chunk size; the update kernel's load phasing
+    (0 = built-in rule, > 0 = device-wide rate in GB/s, < 0 = off)."""
     decay_before_update: bool = False
     clip_eps: float = 0.0
     moments_bf16: bool = False
@@ -127,11 +129,13 @@ class Options:
     capturable: bool = False
     inject_wait_timeout: bool = False    # failure testing: the update kernel's waits run out
     host_chunk: int = 0                  # host-buffer steps: parameters per chunk (0 = default)
+    load_phase_gbs: float = 0.0          # update-kernel load phasing: 0 built-in, > 0 rate (GB/s), < 0 off
 
     def _c(self) -> _COptions:
         return _COptions(C.sizeof(_COptions), 1 if self.decay_before_update else 0, self.clip_eps,
                          1 if self.moments_bf16 else 0, self.bucket_ctas, self.small_step,
-                         1 if self.capturable else 0, 1 if self.inject_wait_timeout else 0, self.host_chunk)
+                         1 if self.capturable else 0, 1 if self.inject_wait_timeout else 0, self.host_chunk,
+                         self.load_phase_gbs)
 
 
 _lib = None

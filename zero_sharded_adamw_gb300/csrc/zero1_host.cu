@@ -353,6 +353,7 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         if (opts->capturable != 0 && opts->capturable != 1) return fail(ZERO1_EINVAL, "capturable must be 0 or 1");
         if (opts->inject_wait_timeout != 0 && opts->inject_wait_timeout != 1)
             return fail(ZERO1_EINVAL, "inject_wait_timeout must be 0 or 1");
+        if (!std::isfinite(opts->load_phase_gbs)) return fail(ZERO1_EINVAL, "load_phase_gbs must be finite");
         o = *opts;
     }
 
@@ -478,6 +479,7 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.small_vpt = zero1::small_step_vpt(h->n, h->world, h->opts.small_step);
     s.dev = dev_scalars(h);
     s.stall_test = h->opts.inject_wait_timeout != 0;
+    s.load_rate_gbs = zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
@@ -544,6 +546,7 @@ int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *con
     zero1::plan_grids(count, false, h->num_sms, &s.grid_rs, &s.grid_update);
     if (max_ctas > 0 && s.grid_update > max_ctas) s.grid_update = max_ctas;
     s.moments_bf16 = h->opts.moments_bf16 != 0;
+    s.load_rate_gbs = zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
     s.phase = 2;

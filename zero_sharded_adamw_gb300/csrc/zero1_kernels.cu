@@ -170,6 +170,7 @@ struct UpdParams {
     DevScalars dev;              // capturable: scalars formed from the device step counter
     int advance_t;               // capturable: this launch ends the step (advances the counter)
     int stall_test;              // failure test: the producer issues nothing, so every wait runs out
+    unsigned long long load_period_ns;  // > 0: each tile's loads wait for the next boundary of this period
 };
 
 // Scalar rank-ordered sum for the last n % 8 parameters.
@@ -649,6 +650,17 @@ zero1_adamw_ag_kernel(const __grid_constant__ UpdParams<CAP> p)
                 const int64_t j = tile_at(k);
                 const int s = k % kUpdStages;
                 if (k >= kUpdStages && !mbar_wait(&sm.empty[s], ((k / kUpdStages) & 1u) ^ 1u, abort, &p.status->errors)) break;
+                if (p.load_period_ns && k >= kUpdStages) {
+                    // Load phasing: once the ring is primed, a tile's loads go
+                    // out only at the next boundary of a period shared by every
+                    // SM (the global nanosecond clock), so the whole grid's
+                    // loads reach DRAM together rather than one by one among
+                    // the stores.  The boundary is at most one period away;
+                    // the iteration cap only guards against a stopped clock.
+                    const unsigned long long next = (global_ns() / p.load_period_ns + 1) * p.load_period_ns;
+                    for (uint32_t it = 0; global_ns() < next && it < (1u << 20); ++it) {
+                    }
+                }
                 const uint64_t base = (uint64_t)j * kUpdTile;
                 const uint32_t cnt = (uint32_t)(nel - base < (uint64_t)kUpdTile ? nel - base : kUpdTile);
                 const uint32_t gbytes = REREAD ? (uint32_t)nw * cnt * 2u : cnt * 4u;
@@ -1115,6 +1127,13 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
                                        : sizeof(UpdSmem<U0.tile, U0.stages>);
     const int k2_threads = (path == 1 ? C1 : path == 2 ? C2 : C0) * 32 + 64;
     if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
+    // Load phasing (fp32 scratch, fp32 moments): the period is the time one
+    // tile's bytes per CTA take when the whole grid moves them at the given
+    // device-wide rate (bytes / (GB/s) = ns).
+    if (path == 1 && s.load_rate_gbs > 0.0) {
+        const double tile_bytes = (28.0 + 2.0 * s.world) * U1.tile;
+        up.load_period_ns = (unsigned long long)(tile_bytes * s.grid_update / s.load_rate_gbs + 0.5);
+    }
     // A whole step without profiling events between its kernels launches
     // both with a programmatic dependency on the kernel before them in the
     // stream: each may launch while its predecessor drains and waits for it
