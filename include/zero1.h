@@ -155,10 +155,12 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     period is the time one tile's bytes take when the grid moves them at
  *     a device-wide rate: 0 = the built-in rate (6800 GB/s up to W = 32,
  *     rising to 7100 at W = 64; phasing off outside 24 <= W <= 64), > 0 =
- *     this rate in GB/s for any W on that path, < 0 = never.  Only launches
- *     whose grid spans every SM are phased (not zero1_bucket_update with
- *     bucket_ctas, nor small pieces).  Timing only: results are the same
- *     bit for bit.  Must be finite.
+ *     this rate in GB/s for any W on that path, < 0 = never.  Only update
+ *     launches that have the device to themselves and span every SM are
+ *     phased: zero1_step's and zero1_bucket_finish's, not
+ *     zero1_bucket_update's (beside a backward) nor the host-buffer steps'
+ *     pieces (beside the next step's reduces and the copies).  Timing
+ *     only: results are the same bit for bit.  Must be finite.
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;

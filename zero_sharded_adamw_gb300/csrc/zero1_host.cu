@@ -526,9 +526,14 @@ int launch_rs_piece(zero1_ctx *h, uint64_t offset, uint64_t count, const void *c
 // offset+count) (the update kernel, c formed from the first nsums norm
 // partials in order): the replicas go to param_ptrs, whose entries point at
 // that range.  capturable: the step scalars come from the device counter,
-// which this launch advances only if advance_t.
+// which this launch advances only if advance_t.  alone: nothing else of the
+// library's runs beside this launch, so the update kernel's load phasing
+// (a period set for the whole device's bandwidth) may apply; the host path's
+// pieces share the device with the next step's reduces and the copies, and
+// a per-bucket update with the caller's backward.
 int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *const *param_ptrs, float *ghat,
-                        double *sums, int nsums, bool capturable, bool advance_t, int max_ctas, cudaStream_t st)
+                        double *sums, int nsums, bool capturable, bool advance_t, int max_ctas, bool alone,
+                        cudaStream_t st)
 {
     zero1::StepLaunch s;
     s.grads = nullptr;
@@ -546,7 +551,9 @@ int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *con
     zero1::plan_grids(count, false, h->num_sms, &s.grid_rs, &s.grid_update);
     if (max_ctas > 0 && s.grid_update > max_ctas) s.grid_update = max_ctas;
     s.moments_bf16 = h->opts.moments_bf16 != 0;
-    s.load_rate_gbs = zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
+    if (alone)
+        s.load_rate_gbs =
+            zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
     s.phase = 2;
@@ -675,7 +682,7 @@ int host_step(zero1_ctx *h, const void *const *host_grads, void *const *host_par
         char *base = ring + (uint64_t)(kHostSlots + sl) * slot_bytes;
         if (P.down_used[sl]) HOST_CHECK(cudaStreamWaitEvent(P.upd, P.down_free[sl], 0), "cudaStreamWaitEvent");
         for (int r = 0; r < W; ++r) pslot[r] = base + (uint64_t)r * P.rank_stride;
-        if ((rc = launch_update_piece(h, lo, cnt, pslot, ghat, sums, M, capturable, i == M - 1, 0, P.upd)))
+        if ((rc = launch_update_piece(h, lo, cnt, pslot, ghat, sums, M, capturable, i == M - 1, 0, false, P.upd)))
             return rc;
         HOST_CHECK(cudaEventRecord(P.upd_done[i], P.upd), "cudaEventRecord");
         P.upd_recorded[i] = 1;
@@ -1048,7 +1055,7 @@ int zero1_bucket_update(zero1_handle h, uint64_t offset, uint64_t count, const v
     // The update of the bucket's parameters right away (c = 1 without
     // clipping); CTA 0 also records the norm of the buckets so far.
     if ((rc = launch_update_piece(h, offset, count, param_ptrs, h->ghat ? h->ghat : h->ghat_bucket, h->bucket_sums,
-                                  (int)h->buckets.size() + 1, false, true, h->opts.bucket_ctas, st)))
+                                  (int)h->buckets.size() + 1, false, true, h->opts.bucket_ctas, false, st)))
         return rc;
     h->buckets.emplace_back(offset, count);
     h->bucket_mode = 2;
@@ -1085,7 +1092,7 @@ int zero1_bucket_finish(zero1_handle h, void *const *param_ptrs, void *stream)
     }
     DeviceGuard g(h->device);
     int rc = launch_update_piece(h, 0, h->n, param_ptrs, h->ghat ? h->ghat : h->ghat_bucket, h->bucket_sums,
-                                 (int)h->buckets.size(), true, true, 0, static_cast<cudaStream_t>(stream));
+                                 (int)h->buckets.size(), true, true, 0, true, static_cast<cudaStream_t>(stream));
     if (rc) return rc;
     h->bucket_open = false;
     h->t += 1;

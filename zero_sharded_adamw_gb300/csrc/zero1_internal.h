@@ -91,7 +91,8 @@ struct StepLaunch {
 // built-in rate where phasing is known to pay, > 0 = this rate, < 0 =
 // never).  Phasing needs every SM in the grid (a period shared by fewer
 // CTAs, or by CTAs that share the device with other work, is not the one
-// measured) and applies to the fp32-scratch, fp32-moment update only.
+// measured; callers whose launch runs beside other work pass no rate) and
+// applies to the fp32-scratch, fp32-moment update only.
 // Built-in: on for 24 <= W <= 64, where the replica stores outweigh the
 // 16 bytes of loads per parameter by 3 to 9 times; the rate that measured
 // best on GB300 rises from 6800 GB/s at W <= 32 to 7100 at W = 64.
