@@ -93,15 +93,16 @@ struct StepLaunch {
 // CTAs, or by CTAs that share the device with other work, is not the one
 // measured; callers whose launch runs beside other work pass no rate) and
 // applies to the fp32-scratch, fp32-moment update only.
-// Built-in: on for 24 <= W <= 64, where the replica stores outweigh the
-// 16 bytes of loads per parameter by 3 to 9 times; the rate that measured
-// best on GB300 rises from 6800 GB/s at W <= 32 to 7100 at W = 64.
+// Built-in: on from W = 24, where the replica stores outweigh the 16 bytes
+// of loads per parameter by 3 times or more; the rate that measured best on
+// GB300 rises from 6800 GB/s at W <= 32 to 7100 at W = 64 and stays near
+// 7100 up to W = 512.
 inline double load_rate_gbs(double option, int world, bool moments_bf16, int grid, int num_sms)
 {
     if (option < 0.0 || moments_bf16 || num_sms <= 0 || grid < num_sms) return 0.0;
     if (option > 0.0) return option;
-    if (world < 24 || world > 64) return 0.0;
-    const double f = world <= 32 ? 0.0 : (world - 32) / 32.0;
+    if (world < 24) return 0.0;
+    const double f = world <= 32 ? 0.0 : world >= 64 ? 1.0 : (world - 32) / 32.0;
     return 6800.0 + 300.0 * f;
 }
 
