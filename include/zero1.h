@@ -144,18 +144,18 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     to a multiple of 2048 (at least 2048); at most 65,536 chunks.
  *   load_phase_gbs: load phasing of the update kernel.  Where the replica
  *     stores far outweigh the loads (the fp32-scratch step with fp32
- *     moments at W >= 24: 16 bytes loaded against 12 + 2W stored per
+ *     moments at W >= 16: 16 bytes loaded against 12 + 2W stored per
  *     parameter), loads issued one tile at a time by each SM reach DRAM
  *     scattered among the stores and cost more than their bytes.  Phased,
  *     each CTA issues a tile's loads only at the next boundary of a period
  *     that every SM shares (the global nanosecond clock), so the grid's
- *     loads arrive together (measured on GB300: the update 3.9% faster at
- *     W = 24, 5.8% at 32, 9.1% at 48, 10-12% at 64 to 256, 6% at 512; at
- *     W = 16 and below it is slower, so it stays off).  The period is the
- *     time one tile's bytes take when the grid moves them at a device-wide
- *     rate: 0 = the built-in rate (6800 GB/s up to W = 32, rising to 7100
- *     at W = 64 and above; phasing off below W = 24), > 0 = this rate in
- *     GB/s for any W on that path, < 0 = never.  Only update
+ *     loads arrive together (measured on GB300: the update 3.7% faster at
+ *     W = 16, 4-6% at 20 to 32, 9% at 48, 8-13% at 64 to 256, 6% at 512;
+ *     below W = 16 every period tried was slower, so it stays off).  The
+ *     period is the time one tile's bytes take when the grid moves them at
+ *     a device-wide rate: 0 = the built-in rule (14000 GB/s, half a tile's
+ *     time, at 16 <= W < 20; 7000 GB/s from W = 20; off below W = 16),
+ *     > 0 = this rate in GB/s for any W on that path, < 0 = never.  Only update
  *     launches that have the device to themselves and span every SM are
  *     phased: zero1_step's and zero1_bucket_finish's, not
  *     zero1_bucket_update's (beside a backward) nor the host-buffer steps'

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libzero1.so")
 SOURCES = ["zero1_host.cu", "zero1_kernels.cu", "zero1_noalloc.cu", "zero1_allreduce.cu", "zero1_partition.cu"]
-HEADERS = [os.path.join(CSRC, "zero1_internal.h"), os.path.join(CSRC, "zero1_ptx.cuh"), os.path.join(INCLUDE, "zero1.h")]
+HEADERS = [os.path.join(CSRC, "zero1_internal.h"), os.path.join(CSRC, "zero1_ptx.cuh"), os.path.join(CSRC, "zero1_policy.h"),
+           os.path.join(INCLUDE, "zero1.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -28,6 +28,7 @@
 
 #include "zero1.h"
 #include "zero1_internal.h"
+#include "zero1_policy.h"
 
 // Slots in each of the host path's two device rings (uploads, downloads),
 // and the copy streams each direction's chunks are dealt over (one copy

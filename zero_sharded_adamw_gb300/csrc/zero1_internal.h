@@ -86,26 +86,6 @@ struct StepLaunch {
     double load_rate_gbs = 0.0;  // > 0: the update kernel's loads phased for this device-wide rate
 };
 
-// The device-wide rate (GB/s) that sets the update kernel's load period, or
-// 0 for free-running loads.  option: zero1_options.load_phase_gbs (0 = the
-// built-in rate where phasing is known to pay, > 0 = this rate, < 0 =
-// never).  Phasing needs every SM in the grid (a period shared by fewer
-// CTAs, or by CTAs that share the device with other work, is not the one
-// measured; callers whose launch runs beside other work pass no rate) and
-// applies to the fp32-scratch, fp32-moment update only.
-// Built-in: on from W = 24, where the replica stores outweigh the 16 bytes
-// of loads per parameter by 3 times or more; the rate that measured best on
-// GB300 rises from 6800 GB/s at W <= 32 to 7100 at W = 64 and stays near
-// 7100 up to W = 512.
-inline double load_rate_gbs(double option, int world, bool moments_bf16, int grid, int num_sms)
-{
-    if (option < 0.0 || moments_bf16 || num_sms <= 0 || grid < num_sms) return 0.0;
-    if (option > 0.0) return option;
-    if (world < 24) return 0.0;
-    const double f = world <= 32 ? 0.0 : world >= 64 ? 1.0 : (world - 32) / 32.0;
-    return 6800.0 + 300.0 * f;
-}
-
 // The one-launch path for small n: a cluster of kSmallCtas CTAs of
 // kSmallThreads threads, each thread holding up to kSmallMaxVpt vectors.
 #ifndef ZERO1_SMALL_CTAS

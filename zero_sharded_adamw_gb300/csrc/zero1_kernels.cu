@@ -30,7 +30,7 @@
 //  - K2 has a store warp whose lanes write the tile's master, m, v and W
 //    bf16 replicas back with bulk stores, so the W-way all-gather costs the
 //    SM one bulk instruction per replica per tile;
-//  - where the stores far outweigh the loads (W >= 24), K2's producer
+//  - where the stores far outweigh the loads (W >= 16), K2's producer
 //    issues each tile's loads at the next boundary of a clock period that
 //    every SM shares, so the grid's loads reach DRAM together instead of
 //    one tile at a time among the stores (load phasing).

@@ -44,6 +44,7 @@
 
 #include "zero1.h"
 #include "zero1_internal.h"
+#include "zero1_policy.h"
 
 namespace {
 

@@ -1,0 +1,31 @@
+// zero1_policy.h -- host-side choices about how a launch runs (never what
+// it computes), shared by the C-ABI host code (zero1_host.cu,
+// zero1_noalloc.cu).  Not installed.
+#pragma once
+
+namespace zero1 {
+
+// The device-wide rate (GB/s) that sets the update kernel's load period, or
+// 0 for free-running loads.  option: zero1_options.load_phase_gbs (0 = the
+// built-in rule, > 0 = this rate, < 0 = never).  Phasing needs every SM in
+// the grid (a period shared by fewer CTAs, or by CTAs that share the device
+// with other work, is not the one measured; callers whose launch runs
+// beside other work pass no rate) and applies to the fp32-scratch,
+// fp32-moment update only.
+//
+// Built-in rule, from sweeps on GB300 (update-kernel time against
+// free-running loads): below W = 16 the loads are too large a share of the
+// bytes (16 against 12 + 2W stored per parameter) and every period tried was
+// slower; at 16 <= W < 20 a period of half a tile's time (14000 GB/s) was
+// 3.7% faster and a whole tile's barely faster; from W = 20 a whole tile's
+// time at 7000 GB/s was 4-13% faster and within about 2% of the best rate
+// on every box measured.
+inline double load_rate_gbs(double option, int world, bool moments_bf16, int grid, int num_sms)
+{
+    if (option < 0.0 || moments_bf16 || num_sms <= 0 || grid < num_sms) return 0.0;
+    if (option > 0.0) return option;
+    if (world < 16) return 0.0;
+    return world < 20 ? 14000.0 : 7000.0;
+}
+
+}  // namespace zero1
