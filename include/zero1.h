@@ -160,7 +160,9 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     phased: zero1_step's and zero1_bucket_finish's, not
  *     zero1_bucket_update's (beside a backward) nor the host-buffer steps'
  *     pieces (beside the next step's reduces and the copies).  Timing
- *     only: results are the same bit for bit.  Must be finite.
+ *     only: results are the same bit for bit.  Must be finite, and a
+ *     positive rate at least 1000 GB/s (a slower one would only stretch
+ *     the step).
  *   size: sizeof(zero1_options) (lets the struct grow). */
 typedef struct zero1_options {
     uint32_t size;
@@ -179,7 +181,7 @@ typedef struct zero1_options {
  * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
  * negative or non-finite clip_eps, a negative bucket_ctas, small_step
  * outside {-1, 0, 1}, capturable or inject_wait_timeout outside {0, 1}, a
- * non-finite load_phase_gbs, and a capturable handle whose bias corrections would need more than 2^22
+ * non-finite load_phase_gbs or one in (0, 1000), and a capturable handle whose bias corrections would need more than 2^22
  * table entries.  All option checks come before any device call. */
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
                     zero1_handle *out);

@@ -164,7 +164,7 @@ def test_options_checked_before_the_device(lib_path):
     h = C.c_void_p()
     for field, value in (("size", 8), ("small_step", 2), ("capturable", 3), ("inject_wait_timeout", 2),
                          ("bucket_ctas", -1), ("clip_eps", -1.0), ("load_phase_gbs", float("nan")),
-                         ("load_phase_gbs", float("inf"))):
+                         ("load_phase_gbs", float("inf")), ("load_phase_gbs", 0.001), ("load_phase_gbs", 999.0)):
         opts = z.Options()._c()
         setattr(opts, field, value)
         assert lib.zero1_create_ex(4096, 4, C.byref(hp), C.byref(opts), C.byref(h)) == -1, field

@@ -355,6 +355,8 @@ int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_
         if (opts->inject_wait_timeout != 0 && opts->inject_wait_timeout != 1)
             return fail(ZERO1_EINVAL, "inject_wait_timeout must be 0 or 1");
         if (!std::isfinite(opts->load_phase_gbs)) return fail(ZERO1_EINVAL, "load_phase_gbs must be finite");
+        if (opts->load_phase_gbs > 0.0 && opts->load_phase_gbs < 1000.0)
+            return fail(ZERO1_EINVAL, "load_phase_gbs must be <= 0 or at least 1000 (GB/s), got %g", opts->load_phase_gbs);
         o = *opts;
     }
 
