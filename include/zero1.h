@@ -154,8 +154,11 @@ int zero1_create(uint64_t n, int world, const zero1_hparams *hp, zero1_handle *o
  *     below W = 16 every period tried was slower, so it stays off).  The
  *     period is the time one tile's bytes take when the grid moves them at
  *     a device-wide rate: 0 = the built-in rule (14000 GB/s, half a tile's
- *     time, at 16 <= W < 20; 7000 GB/s from W = 20; off below W = 16),
- *     > 0 = this rate in GB/s for any W on that path, < 0 = never.  Only update
+ *     time, at 16 <= W < 20; 7000 GB/s from W = 20; off below W = 16; and
+ *     17500 GB/s, about 0.4 of a tile's time, for the W <= 2 step that
+ *     re-reads the gradients, 16 bytes in and 16 out per parameter, where
+ *     it measured 1.2% faster), > 0 = this rate in GB/s for any W on
+ *     either path, < 0 = never.  Only update
  *     launches that have the device to themselves and span every SM are
  *     phased: zero1_step's and zero1_bucket_finish's, not
  *     zero1_bucket_update's (beside a backward) nor the host-buffer steps'

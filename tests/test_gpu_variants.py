@@ -182,10 +182,11 @@ def test_bf16_moments_range_checkpoint():
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
-@pytest.mark.parametrize("world,rate", [(16, 0.0), (24, 0.0), (64, 0.0), (128, 0.0), (8, 6500.0)])
+@pytest.mark.parametrize("world,rate", [(2, 0.0), (16, 0.0), (24, 0.0), (64, 0.0), (128, 0.0), (8, 6500.0)])
 def test_load_phasing_is_timing_only(world, rate):
-    """The update kernel with phased loads (the built-in rule at W = 16, 24,
-    64 and 128, an explicit device-wide rate at W = 8; 1M parameters, so the
+    """The update kernel with phased loads (the built-in rule at W = 2 on the
+    gradient re-read path and at W = 16, 24, 64 and 128 on the scratch path,
+    an explicit device-wide rate at W = 8; 1M parameters, so the
     grid spans every SM) computes what the free-running kernel computes, bit
     for bit, and what the oracle computes with the step's clip coefficient
     injected, over three steps."""

@@ -482,7 +482,8 @@ int zero1_step(zero1_handle h, const void *const *grad_ptrs, void *const *param_
     s.small_vpt = zero1::small_step_vpt(h->n, h->world, h->opts.small_step);
     s.dev = dev_scalars(h);
     s.stall_test = h->opts.inject_wait_timeout != 0;
-    s.load_rate_gbs = zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
+    s.load_rate_gbs = zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, h->ghat == nullptr,
+                                           s.grid_update, h->num_sms);
     cudaEvent_t *ev = nullptr;
     if (h->prof_used < h->prof_capacity) ev = &h->prof[3 * (size_t)h->prof_used];
     cudaError_t e = zero1::launch_step(s, static_cast<cudaStream_t>(stream), ev);
@@ -556,7 +557,7 @@ int launch_update_piece(zero1_ctx *h, uint64_t offset, uint64_t count, void *con
     s.moments_bf16 = h->opts.moments_bf16 != 0;
     if (alone)
         s.load_rate_gbs =
-            zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, s.grid_update, h->num_sms);
+            zero1::load_rate_gbs(h->opts.load_phase_gbs, h->world, s.moments_bf16, false, s.grid_update, h->num_sms);
     s.decay_first = h->opts.decay_before_update != 0;
     s.clip_eps = h->opts.clip_eps;
     s.phase = 2;

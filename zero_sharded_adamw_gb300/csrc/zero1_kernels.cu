@@ -1131,11 +1131,14 @@ cudaError_t launch_w(const StepLaunch &s, cudaStream_t stream, cudaEvent_t *ev)
                                        : sizeof(UpdSmem<U0.tile, U0.stages>);
     const int k2_threads = (path == 1 ? C1 : path == 2 ? C2 : C0) * 32 + 64;
     if ((e = allow_smem(k2, k2_smem)) != cudaSuccess) return e;
-    // Load phasing (fp32 scratch, fp32 moments): the period is the time one
-    // tile's bytes per CTA take when the whole grid moves them at the given
-    // device-wide rate (bytes / (GB/s) = ns).
-    if (path == 1 && s.load_rate_gbs > 0.0) {
-        const double tile_bytes = (28.0 + 2.0 * s.world) * U1.tile;
+    // Load phasing (fp32 moments; the scratch path or the gradient re-read
+    // path): the period is the time one tile's bytes per CTA take when the
+    // whole grid moves them at the given device-wide rate (bytes / (GB/s) =
+    // ns).  A tile moves 28 + 2W bytes per parameter on the scratch path
+    // (ĝ, master, m, v in; master, m, v, W replicas out) and 24 + 4W on the
+    // re-read path (W gradients in instead of ĝ).
+    if (path != 2 && s.load_rate_gbs > 0.0) {
+        const double tile_bytes = path == 1 ? (28.0 + 2.0 * s.world) * U1.tile : (24.0 + 4.0 * s.world) * U0.tile;
         up.load_period_ns = (unsigned long long)(tile_bytes * s.grid_update / s.load_rate_gbs + 0.5);
     }
     // A whole step without profiling events between its kernels launches

@@ -194,7 +194,7 @@ extern "C" int zero1_step_noalloc(uint64_t n, int world, const zero1_hparams *hp
     s.max_norm = hp->max_norm;
     s.small_vpt = zero1::small_step_vpt(n, world, 0);
     zero1::plan_grids(n, reread, num_sms, &s.grid_rs, &s.grid_update);
-    s.load_rate_gbs = zero1::load_rate_gbs(0.0, world, false, s.grid_update, num_sms);
+    s.load_rate_gbs = zero1::load_rate_gbs(0.0, world, false, reread, s.grid_update, num_sms);
     if ((size_t)s.grid_rs * 2 > kPartialDoubles)
         return nfail(ZERO1_EINVAL, "grid of %d CTAs exceeds the fixed partials scratch", s.grid_rs);
 
