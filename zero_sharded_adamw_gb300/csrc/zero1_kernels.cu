@@ -33,7 +33,8 @@
 //  - where the stores far outweigh the loads (W >= 16), K2's producer
 //    issues each tile's loads at the next boundary of a clock period that
 //    every SM shares, so the grid's loads reach DRAM together instead of
-//    one tile at a time among the stores (load phasing).
+//    one tile at a time among the stores (load phasing); the W <= 2
+//    re-read path uses the same gate with a period of about 0.4 tile.
 // Every mbarrier wait gives up after 1 s of global time: it raises the CTA's
 // abort flag and a sticky error bit in the status the host reads; a producer
 // that stops lets its loads in flight land before exiting.
