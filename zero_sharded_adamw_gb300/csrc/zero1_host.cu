@@ -31,8 +31,11 @@
 #include "zero1_policy.h"
 
 // Slots in each of the host path's two device rings (uploads, downloads),
-// and the copy streams each direction's chunks are dealt over (one copy
-// engine each, so that several run at once).
+// and the copy streams each direction's chunks are dealt over, so that
+// several copies are in flight (the driver maps the streams onto the
+// device's copy engines; GB300 reports three).  Measured on the 7B
+// workload: 8 or 16 slots with 2, 3 or 4 streams run at the same host-link
+// rate within a few percent.
 #ifndef ZERO1_HOST_SLOTS
 #define ZERO1_HOST_SLOTS 8
 #define ZERO1_HOST_COPY_STREAMS 4
