@@ -34,9 +34,9 @@
 // and the copy streams each direction's chunks are dealt over, so that
 // several copies are in flight (the driver maps the streams onto the
 // device's copy engines; GB300 reports three).  Measured on the 7B
-// workload: 8 or 16 slots with 2 or 4 streams, and 16 with 3, ran within 7%
-// of one another (the host link sets the rate); 8 slots with 3 streams
-// were about 10% slower.
+// workload: 8 or 16 slots with 2 or 4 streams ran within 7% of one another
+// (the host link sets the rate); 8 slots with 3 streams were about 10%
+// slower.
 #ifndef ZERO1_HOST_SLOTS
 #define ZERO1_HOST_SLOTS 8
 #define ZERO1_HOST_COPY_STREAMS 4
