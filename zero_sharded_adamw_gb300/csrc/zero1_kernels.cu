@@ -92,7 +92,7 @@ constexpr RsConfig kRsRead{ZERO1_RS_READ_TILE, ZERO1_RS_READ_RANKS, ZERO1_RS_REA
 // The update kernel's tile, ring depth, consumer warps and tile order, per
 // path (measured on GB300, gpt2_small / ragged / 7B / W = 64 / bf16-moment
 // workloads):
-//  - fp32 scratch, fp32 moments: write-heavy (16 B read, 24 + 2W written per
+//  - fp32 scratch, fp32 moments: write-heavy (16 B read, 12 + 2W written per
 //    parameter); fastest with 2048-parameter tiles, 3 stages in flight and 16
 //    consumer warps, tiles grid-strided;
 //  - fp32 scratch, bf16 moments: 2048-parameter tiles, 4 stages, 8 warps;
