@@ -40,3 +40,13 @@ def test_measured_peak(tmp_path, monkeypatch):
     assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 1234.5}))
     assert bench.measured_peak() == (1234.5, "measured")
+
+
+def test_digest_covers_the_kernel_sources_only():
+    """The digest that ties ncu summaries to the code covers what the kernels
+    compile from, and not host-side launch policy (zero1_policy.h), whose
+    retuning changes no kernel."""
+    names = sorted(os.path.basename(p) for p in bench.KERNEL_SRCS)
+    assert names == ["zero1_internal.h", "zero1_kernels.cu", "zero1_ptx.cuh"]
+    kernels = open(os.path.join(bench.CSRC, "zero1_kernels.cu")).read()
+    assert '#include "zero1_policy.h"' not in kernels
