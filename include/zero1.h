@@ -184,8 +184,9 @@ typedef struct zero1_options {
  * Errors as zero1_create, plus ZERO1_EINVAL for a bad opts->size, a
  * negative or non-finite clip_eps, a negative bucket_ctas, small_step
  * outside {-1, 0, 1}, capturable or inject_wait_timeout outside {0, 1}, a
- * non-finite load_phase_gbs or one in (0, 1000), and a capturable handle whose bias corrections would need more than 2^22
- * table entries.  All option checks come before any device call. */
+ * non-finite load_phase_gbs or one in (0, 1000), and a capturable handle
+ * whose bias corrections would need more than 2^22 table entries.  All
+ * option checks come before any device call. */
 int zero1_create_ex(uint64_t n, int world, const zero1_hparams *hp, const zero1_options *opts,
                     zero1_handle *out);
 
@@ -312,7 +313,8 @@ int zero1_set_state(zero1_handle h, const float *master, const void *m, const vo
 
 /* Checkpoint save ("Parallel training", "Training loop and checkpoint": a
  * checkpoint must hold m, v and the step count t, or bias correction
- * restarts from t = 1 without the moments): copies master, m, v (n fp32 each) into device or host
+ * restarts from t = 1 without the moments): copies master (n fp32), m and
+ * v (n fp32 each, or bf16 on a moments_bf16 handle) into device or host
  * arrays (any may be NULL to skip it) and writes the step count to *t (may
  * be NULL).  Enqueued on `stream`; synchronize it before reading a host
  * destination.  On a capturable handle t is read from the device counter
