@@ -409,7 +409,8 @@ int zero1_step_scalars(const zero1_hparams *hp, int world, uint64_t t, float out
  * memory, a plug-in whose host fixes its device memory up front, or a loop
  * that cannot take the device synchronisation cudaMalloc/cudaFree imply.
  * The pages have no counterpart to this entry point; it is the same two
- * kernels as zero1_step with the caller owning all state.
+ * kernels as zero1_step with the caller owning all state (and the built-in
+ * load-phasing rule of zero1_options.load_phase_gbs = 0).
  *   n, world, hp: as zero1_create; n is limited to 4,194,304 parameters
  *     (larger n: ZERO1_EINVAL with a message; use zero1_create/zero1_step).
  *   t: this step's number, 1-based (the caller keeps the count).
